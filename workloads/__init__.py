@@ -1,0 +1,194 @@
+"""Seeded synthetic inputs for large-beam decode attention.
+
+This module draws random inputs only. It holds none of the attention
+arithmetic: both the CPU oracle (``oracle/``) and the CUDA path
+(``beam_decode_attention_gb300``) consume what it returns, and neither
+imports the other.
+
+Geometry follows the workloads the GR-Inference blog ("GR-Inference",
+system design section) and the SID-GR Inference README (section 9, Nsight
+breakdown) describe: Qwen3-0.6B / 1.7B / 4B attention heads, beam widths of
+128 to 900, contexts of 1k to 4k tokens, three decode steps, a first step
+that expands from the single prefill row.
+
+Recipe (fixed, so that any two runs draw the same bits):
+
+* ``numpy.random.Generator(PCG64(seed))`` with ``seed = 1000 + index`` where
+  ``index`` is the workload's position in :data:`WORKLOADS`.
+* Draw order: context lengths (ragged workloads only, integers uniform in
+  ``[lc_lo, lc_hi]``), ``ctx_k``, ``ctx_v``, then for each step ``t``:
+  ``beam_k[t]``, ``beam_v[t]``, ``q[t]``, ``parents[t]``.
+* Values are standard normal float32 rounded to bfloat16 (round to nearest,
+  ties to even) and stored as ``uint16`` bit patterns.
+* Parents at step 0 are all 0 (every beam expands from the one prefill row);
+  at step ``t >= 1`` they are uniform in ``[0, W[t-1])``.
+* Storage that no active row may read is poisoned: bf16 NaN for K/V slots
+  past a context length or past the step's width, ``-1`` for unused
+  BeamPath entries.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+@dataclasses.dataclass(frozen=True)
+class WorkloadSpec:
+    name: str
+    num_requests: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    lc: int                     # fixed context length (0 when ragged)
+    lc_range: Optional[tuple]   # (lo, hi) inclusive when ragged
+    widths: tuple               # active beam width per decode step
+    description: str
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def steps(self) -> int:
+        return len(self.widths)
+
+
+WORKLOADS: List[WorkloadSpec] = [
+    WorkloadSpec("tiny_r1_h4x2_d64_lc64_w4", 1, 4, 2, 64, 64, None, (4, 4, 4),
+                 "1 request, Hq=4, Hkv=2, D=64, Lc=64, widths 4/4/4"),
+    WorkloadSpec("qwen3_0.6b_r8_lc1024_w128", 8, 16, 8, 128, 1024, None, (128, 128, 128),
+                 "Qwen3-0.6B heads, 8 requests, Lc=1024, width 128"),
+    WorkloadSpec("qwen3_0.6b_r4_lc2048_w900", 4, 16, 8, 128, 2048, None, (900, 900, 900),
+                 "Qwen3-0.6B heads, 4 requests, Lc=2048, width 900"),
+    WorkloadSpec("qwen3_4b_r4_lc3072_w512", 4, 32, 8, 128, 3072, None, (512, 512, 512),
+                 "Qwen3-4B heads, 4 requests, Lc=3072, width 512"),
+    WorkloadSpec("qwen3_1.7b_r16_lc512-4096_w20-300-900", 16, 16, 8, 128, 0, (512, 4096),
+                 (20, 300, 900),
+                 "Qwen3-1.7B heads, 16 requests, Lc uniform in [512,4096], widths 20/300/900"),
+]
+
+WORKLOAD_BY_NAME: Dict[str, WorkloadSpec] = {w.name: w for w in WORKLOADS}
+# the headline workload: beam width 900 over a 2048-token context
+HEADLINE = WORKLOADS[2].name
+SMALL = WORKLOADS[0].name
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16, nearest-even, returning uint16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    out = ((u + bias) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = BF16_NAN
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+def make_inputs(spec: WorkloadSpec, seed: Optional[int] = None,
+                widths: Optional[Sequence[int]] = None) -> Dict[str, object]:
+    """Draw one workload. Returns a dict of numpy arrays (bf16 as uint16).
+
+    Keys: ``q`` (list per step, ``[R, W_t, Hq, D]``), ``ctx_k``/``ctx_v``
+    (``[R, Hkv, Lc_max, D]``), ``ctx_len`` (``[R]`` int32), ``beam_k``/``beam_v``
+    (``[R, S_max, W_max, Hkv, D]``), ``beam_path`` (``[R, S_max, W_max]``
+    int32), ``widths`` (``[S_max]`` int32) and the shape scalars.
+    """
+    if seed is None:
+        seed = 1000 + WORKLOADS.index(spec)
+    W = tuple(int(w) for w in (widths if widths is not None else spec.widths))
+    R, Hq, Hkv, D = spec.num_requests, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    S = len(W)
+    W_max = max(W)
+    rng = np.random.Generator(np.random.PCG64(seed))
+
+    if spec.lc_range is not None:
+        lo, hi = spec.lc_range
+        ctx_len = rng.integers(lo, hi, size=R, endpoint=True).astype(np.int32)
+    else:
+        ctx_len = np.full(R, spec.lc, dtype=np.int32)
+    lc_max = int(ctx_len.max()) if R else 0
+
+    ctx_k = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    ctx_v = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    for r in range(R):
+        ctx_k[r, :, ctx_len[r]:, :] = BF16_NAN
+        ctx_v[r, :, ctx_len[r]:, :] = BF16_NAN
+
+    beam_k = np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16)
+    beam_v = np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16)
+    beam_path = np.full((R, S, W_max), -1, dtype=np.int32)
+    q = []
+    for t in range(S):
+        beam_k[:, t, :W[t]] = _normal_bf16(rng, (R, W[t], Hkv, D))
+        beam_v[:, t, :W[t]] = _normal_bf16(rng, (R, W[t], Hkv, D))
+        q.append(_normal_bf16(rng, (R, W[t], Hq, D)))
+        if t == 0:
+            beam_path[:, 0, :W[0]] = 0
+        else:
+            beam_path[:, t, :W[t]] = rng.integers(0, W[t - 1], size=(R, W[t])).astype(np.int32)
+
+    return dict(
+        name=spec.name, num_requests=R, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+        ctx_capacity=lc_max, step_capacity=S, beam_capacity=W_max,
+        softmax_scale=float(np.float32(1.0 / np.sqrt(D))),
+        q=q, ctx_k=ctx_k, ctx_v=ctx_v, ctx_len=ctx_len,
+        beam_k=beam_k, beam_v=beam_v, beam_path=beam_path,
+        widths=np.asarray(W, dtype=np.int32),
+    )
+
+
+def make_custom(R: int, Hq: int, Hkv: int, D: int, ctx_len: Sequence[int],
+                widths: Sequence[int], seed: int, lc_max: Optional[int] = None,
+                q_scale: float = 1.0) -> Dict[str, object]:
+    """Same recipe with arbitrary shapes (edge cases in the tests).
+
+    ``q_scale`` multiplies the float32 draw of ``q`` before rounding, which
+    sharpens the softmax so that single keys carry visible weight.
+    """
+    W = tuple(int(w) for w in widths)
+    S = len(W)
+    W_max = max(W)
+    ctx_len = np.asarray(ctx_len, dtype=np.int32)
+    if lc_max is None:
+        lc_max = int(ctx_len.max()) if R else 0
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx_k = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    ctx_v = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    for r in range(R):
+        ctx_k[r, :, ctx_len[r]:, :] = BF16_NAN
+        ctx_v[r, :, ctx_len[r]:, :] = BF16_NAN
+    beam_k = np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16)
+    beam_v = np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16)
+    beam_path = np.full((R, S, W_max), -1, dtype=np.int32)
+    q = []
+    for t in range(S):
+        beam_k[:, t, :W[t]] = _normal_bf16(rng, (R, W[t], Hkv, D))
+        beam_v[:, t, :W[t]] = _normal_bf16(rng, (R, W[t], Hkv, D))
+        q.append(f32_to_bf16_bits(
+            rng.standard_normal(size=(R, W[t], Hq, D), dtype=np.float32) * np.float32(q_scale)))
+        if t == 0:
+            beam_path[:, 0, :W[0]] = 0
+        else:
+            beam_path[:, t, :W[t]] = rng.integers(0, W[t - 1], size=(R, W[t])).astype(np.int32)
+    return dict(
+        name="custom", num_requests=R, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+        ctx_capacity=lc_max, step_capacity=S, beam_capacity=W_max,
+        softmax_scale=float(np.float32(1.0 / np.sqrt(D))),
+        q=q, ctx_k=ctx_k, ctx_v=ctx_v, ctx_len=ctx_len,
+        beam_k=beam_k, beam_v=beam_v, beam_path=beam_path,
+        widths=np.asarray(W, dtype=np.int32),
+    )
