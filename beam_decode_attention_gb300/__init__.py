@@ -1,0 +1,230 @@
+"""Python binding of libgrattn.so: large-beam decode attention on GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/gr_attn.h``.  PyTorch provides
+device memory and streams.  There is no CPU fallback: if the library is
+missing or the device is not an sm_103 GPU, the calls raise.
+
+The functions mirror the C entry points:
+
+* :func:`gr_decode_attn` -- the whole decode attention (shared context stage
+  on tensor cores, per-beam stage along BeamPath, log-sum-exp merge);
+* :func:`gr_decode_attn_workspace_size`;
+* :func:`gr_resolve_ancestors` / :func:`gr_validate_beam_path` -- BeamPath
+  utilities;
+* :func:`gr_get_device_error`, :func:`gr_status_string`.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from . import build as _build
+
+__all__ = [
+    "GRError", "Shape", "load", "lib_path", "gr_decode_attn", "gr_decode_attn_workspace_size",
+    "gr_resolve_ancestors", "gr_validate_beam_path", "gr_get_device_error", "gr_status_string",
+    "gr_version", "EXPORTED_SYMBOLS", "gr_decode_attn_timed", "gr_decode_attn_plan", "PlanInfo",
+]
+
+EXPORTED_SYMBOLS = (
+    "gr_decode_attn_workspace_size", "gr_decode_attn", "gr_decode_attn_timed",
+    "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
+    "gr_get_device_error", "gr_status_string", "gr_version",
+)
+
+GR_OK = 0
+STATUS_NAMES = {
+    0: "GR_OK", -1: "GR_ERR_NULL_ARG", -2: "GR_ERR_BAD_SHAPE", -3: "GR_ERR_UNSUPPORTED",
+    -4: "GR_ERR_MISALIGNED", -5: "GR_ERR_WORKSPACE_TOO_SMALL", -6: "GR_ERR_CUDA",
+    -7: "GR_ERR_DEVICE_TIMEOUT", -8: "GR_ERR_BAD_BEAM_PATH",
+}
+
+
+class GRError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({gr_status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    """``gr_attn_shape``."""
+    _fields_ = [
+        ("num_requests", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("ctx_capacity", ctypes.c_int32),
+        ("step_capacity", ctypes.c_int32),
+        ("beam_capacity", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+    @classmethod
+    def of(cls, d) -> "Shape":
+        return cls(int(d["num_requests"]), int(d["num_q_heads"]), int(d["num_kv_heads"]),
+                   int(d["head_dim"]), int(d["ctx_capacity"]), int(d["step_capacity"]),
+                   int(d["beam_capacity"]), float(d["softmax_scale"]))
+
+
+class PlanInfo(ctypes.Structure):
+    """``gr_plan_info``."""
+    _fields_ = [
+        ("path", ctypes.c_int32),
+        ("n_splits", ctypes.c_int32),
+        ("split_len", ctypes.c_int32),
+        ("context_ctas", ctypes.c_int32),
+        ("kernels", ctypes.c_int32),
+        ("fused_merge", ctypes.c_int32),
+    ]
+
+    def as_dict(self):
+        return {f: int(getattr(self, f)) for f, _ in self._fields_}
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libgrattn.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    sp = ctypes.POINTER(Shape)
+    lib.gr_decode_attn_workspace_size.argtypes = [sp, vp, i32]
+    lib.gr_decode_attn_workspace_size.restype = sz
+    lib.gr_decode_attn.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.gr_decode_attn.restype = ctypes.c_int
+    lib.gr_decode_attn_timed.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz,
+                                         vp, vp]
+    lib.gr_decode_attn_timed.restype = ctypes.c_int
+    lib.gr_decode_attn_plan.argtypes = [sp, vp, i32, ctypes.POINTER(PlanInfo)]
+    lib.gr_decode_attn_plan.restype = ctypes.c_int
+    lib.gr_resolve_ancestors.argtypes = [sp, vp, vp, i32, vp, vp]
+    lib.gr_resolve_ancestors.restype = ctypes.c_int
+    lib.gr_validate_beam_path.argtypes = [sp, vp, vp, i32, vp, vp, vp]
+    lib.gr_validate_beam_path.restype = ctypes.c_int
+    lib.gr_get_device_error.argtypes = []
+    lib.gr_get_device_error.restype = ctypes.c_int
+    lib.gr_status_string.argtypes = [ctypes.c_int]
+    lib.gr_status_string.restype = ctypes.c_char_p
+    lib.gr_version.argtypes = []
+    lib.gr_version.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _widths_arr(widths: Sequence[int]):
+    arr = (ctypes.c_int32 * max(1, len(widths)))(*[int(w) for w in widths])
+    return arr
+
+
+def _ptr(t) -> Optional[int]:
+    """Device/host address of a tensor (None stays NULL)."""
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != GR_OK:
+        raise GRError(rc, where)
+
+
+def gr_status_string(status: int) -> str:
+    return load().gr_status_string(int(status)).decode()
+
+
+def gr_version() -> int:
+    return int(load().gr_version())
+
+
+def gr_decode_attn_workspace_size(shape: Shape, widths: Sequence[int], step: int) -> int:
+    w = _widths_arr(widths)
+    return int(load().gr_decode_attn_workspace_size(ctypes.byref(shape), w, int(step)))
+
+
+def gr_decode_attn(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
+                   widths: Sequence[int], step: int, out, lse, workspace=None,
+                   workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """Enqueue gr_decode_attn on ``stream`` (default: torch's current stream).
+
+    Tensors are torch CUDA tensors laid out as ``include/gr_attn.h`` states
+    (bf16 tensors may be ``torch.bfloat16`` or ``int16`` bit patterns).
+    Raises :class:`GRError` on a non-zero status.
+    """
+    w = _widths_arr(widths)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().gr_decode_attn(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
+                               _ptr(ctx_len), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path), w,
+                               int(step), _ptr(out), _ptr(lse), _ptr(workspace),
+                               int(workspace_bytes), _stream_handle(stream))
+    _check(rc, "gr_decode_attn")
+
+
+def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
+                         widths: Sequence[int], step: int, out, lse, workspace, events,
+                         workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``)
+    before the context kernel, after it, and after the last kernel."""
+    w = _widths_arr(widths)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    for e in events:
+        if e.cuda_event == 0:      # torch creates the event lazily on first record
+            e.record()
+    ev = (ctypes.c_void_p * 3)(*[int(e.cuda_event) for e in events])
+    rc = load().gr_decode_attn_timed(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
+                                     _ptr(ctx_len), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path), w,
+                                     int(step), _ptr(out), _ptr(lse), _ptr(workspace),
+                                     int(workspace_bytes), _stream_handle(stream), ev)
+    _check(rc, "gr_decode_attn_timed")
+
+
+def gr_decode_attn_plan(shape: Shape, widths: Sequence[int], step: int) -> dict:
+    info = PlanInfo()
+    rc = load().gr_decode_attn_plan(ctypes.byref(shape), _widths_arr(widths), int(step),
+                                    ctypes.byref(info))
+    _check(rc, "gr_decode_attn_plan")
+    return info.as_dict()
+
+
+def gr_resolve_ancestors(shape: Shape, beam_path, widths: Sequence[int], step: int, anc,
+                         stream=None) -> None:
+    rc = load().gr_resolve_ancestors(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths),
+                                     int(step), _ptr(anc), _stream_handle(stream))
+    _check(rc, "gr_resolve_ancestors")
+
+
+def gr_validate_beam_path(shape: Shape, beam_path, widths: Sequence[int], step: int, ctx_len,
+                          bad_count, stream=None) -> None:
+    rc = load().gr_validate_beam_path(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths),
+                                      int(step), _ptr(ctx_len), _ptr(bad_count),
+                                      _stream_handle(stream))
+    _check(rc, "gr_validate_beam_path")
+
+
+def gr_get_device_error() -> int:
+    return int(load().gr_get_device_error())

@@ -1,0 +1,351 @@
+// gr_host.cu -- the C ABI of libgrattn.so (include/gr_attn.h): argument
+// checks, the split planner, workspace carve-up and kernel launches.
+//
+// The call follows the three stages of the pages' decode attention: shared
+// (context) stage, unshared (per-beam) stage, log-sum-exp merge (GR-Inference
+// blog, "kernel design"; xGR review, "xAttention").
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gr_attn.h"
+#include "gr_internal.h"
+
+namespace gr {
+
+// Device error word: kernels that give up a bounded wait, or meet a broken
+// precondition, record a code here (see raise_device_error).
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    int *err_ptr = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, looked up once with that device current.
+int device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GR_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GR_ERR_CUDA;
+        }
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return GR_ERR_CUDA;
+        }
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        d.err_ptr = static_cast<int *>(p);
+        d.ready = true;
+    }
+    *out = d;
+    return d.supported ? GR_OK : GR_ERR_UNSUPPORTED;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int make_geometry(const gr_attn_shape *s, const int32_t *widths, int32_t step, Geometry *g) {
+    if (!s || !widths) return GR_ERR_NULL_ARG;
+    if (s->num_requests < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->ctx_capacity < 0 ||
+        s->step_capacity < 1 || s->beam_capacity < 1)
+        return GR_ERR_BAD_SHAPE;
+    if (s->num_q_heads % s->num_kv_heads != 0) return GR_ERR_BAD_SHAPE;
+    if (s->head_dim != 64 && s->head_dim != 128) return GR_ERR_UNSUPPORTED;
+    if (s->num_q_heads / s->num_kv_heads > 128) return GR_ERR_UNSUPPORTED;
+    if (!(std::isfinite(s->softmax_scale))) return GR_ERR_BAD_SHAPE;
+    if (step < 0 || step >= s->step_capacity) return GR_ERR_BAD_SHAPE;
+    if (step >= kMaxSteps) return GR_ERR_UNSUPPORTED;
+    std::memset(g, 0, sizeof *g);
+    for (int t = 0; t <= step; ++t) {
+        if (widths[t] < 1 || widths[t] > s->beam_capacity) return GR_ERR_BAD_SHAPE;
+        g->widths[t] = widths[t];
+    }
+    g->R = s->num_requests;
+    g->Hq = s->num_q_heads;
+    g->Hkv = s->num_kv_heads;
+    g->G = s->num_q_heads / s->num_kv_heads;
+    g->D = s->head_dim;
+    g->Lc_max = s->ctx_capacity;
+    g->S_max = s->step_capacity;
+    g->W_max = s->beam_capacity;
+    g->step = step;
+    g->W_s = widths[step];
+    g->scale = s->softmax_scale;
+    g->scale_log2 = s->softmax_scale * 1.4426950408889634f;
+    // every index the kernels form must fit comfortably in 64-bit arithmetic
+    // and every grid dimension in its hardware limit
+    const double rows = (double)g->R * g->W_s * g->Hq;
+    if (rows * g->D > 4.0e15 || (double)g->R * g->Hkv > 65535.0) return GR_ERR_BAD_SHAPE;
+    return GR_OK;
+}
+
+enum class Path { kTensorCore, kSimt };
+
+Path chosen_path() {
+    const char *e = std::getenv("GR_ATTN_FORCE_PATH");
+    if (e && std::strcmp(e, "simt") == 0) return Path::kSimt;
+    return Path::kSimt;
+}
+
+int forced_splits() {
+    const char *e = std::getenv("GR_ATTN_FORCE_SPLITS");
+    if (!e) return 0;
+    int v = std::atoi(e);
+    return v > 0 ? v : 0;
+}
+
+// Split plan for the CUDA-core context stage.
+SplitPlan plan_simt(const Geometry &g, int sm_count) {
+    SplitPlan p{0, 0};
+    if (g.Lc_max == 0) return p;
+    constexpr int kKeyBlock = 32;
+    const int blocks = (g.Lc_max + kKeyBlock - 1) / kKeyBlock;
+    const long long ctas = (long long)((g.W_s * g.G + 15) / 16) * g.R * g.Hkv;
+    int n = forced_splits();
+    if (n == 0) {
+        const long long target = 4LL * sm_count;
+        n = (int)std::min<long long>(blocks, std::max<long long>(1, (target + ctas - 1) / ctas));
+    }
+    n = std::min(n, blocks);
+    const int per = (blocks + n - 1) / n;
+    p.split_len = per * kKeyBlock;
+    p.n_splits = (g.Lc_max + p.split_len - 1) / p.split_len;
+    return p;
+}
+
+SplitPlan plan(const Geometry &g, int sm_count) { return plan_simt(g, sm_count); }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t part_o, part_lse, total;
+};
+
+Layout workspace_layout(const Geometry &g, const SplitPlan &p) {
+    Layout l{0, 0, 0};
+    const size_t rows = (size_t)g.R * g.W_s * g.Hq;
+    const size_t o_bytes = (size_t)p.n_splits * rows * g.D * sizeof(float);
+    const size_t lse_bytes = (size_t)p.n_splits * rows * sizeof(float);
+    l.part_o = 0;
+    l.part_lse = align256(o_bytes);
+    l.total = p.n_splits ? align256(l.part_lse + lse_bytes) : 0;
+    return l;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GR_OK;
+    cudaGetLastError();
+    return GR_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gr
+
+using namespace gr;
+
+extern "C" {
+
+int gr_version(void) { return 100; }
+
+const char *gr_status_string(int status) {
+    switch (status) {
+        case GR_OK: return "ok";
+        case GR_ERR_NULL_ARG: return "a required pointer is NULL";
+        case GR_ERR_BAD_SHAPE: return "inconsistent or out-of-range sizes";
+        case GR_ERR_UNSUPPORTED: return "unsupported head_dim, head grouping or device";
+        case GR_ERR_MISALIGNED: return "a device pointer is not 16-byte aligned";
+        case GR_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than gr_decode_attn_workspace_size()";
+        case GR_ERR_CUDA: return "a CUDA call failed";
+        case GR_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+        case GR_ERR_BAD_BEAM_PATH: return "a BeamPath parent slot was out of range";
+        default: return "unknown status";
+    }
+}
+
+size_t gr_decode_attn_workspace_size(const gr_attn_shape *shape, const int32_t *widths, int32_t step) {
+    Geometry g;
+    if (make_geometry(shape, widths, step, &g) != GR_OK) return 0;
+    DeviceInfo dev;
+    if (device_info(&dev) != GR_OK) return 0;
+    return workspace_layout(g, plan(g, dev.sm_count)).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+               const int32_t *ctx_len, const void *beam_k, const void *beam_v,
+               const int32_t *beam_path, const int32_t *widths, int32_t step, void *out, float *lse,
+               void *workspace, size_t workspace_bytes, gr_stream_t stream,
+               gr_event_t const *events) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!q || !ctx_len || !beam_k || !beam_v || !beam_path || !out || !lse) return GR_ERR_NULL_ARG;
+    if (g.Lc_max > 0 && (!ctx_k || !ctx_v)) return GR_ERR_NULL_ARG;
+    if (misaligned(q) || misaligned(ctx_k) || misaligned(ctx_v) || misaligned(ctx_len) ||
+        misaligned(beam_k) || misaligned(beam_v) || misaligned(beam_path) || misaligned(out) ||
+        misaligned(lse) || misaligned(workspace))
+        return GR_ERR_MISALIGNED;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    const SplitPlan sp = plan(g, dev.sm_count);
+    const Layout lay = workspace_layout(g, sp);
+    if (lay.total > 0 && (!workspace || workspace_bytes < lay.total)) return GR_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) -> int {
+        if (!events) return GR_OK;
+        return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s));
+    };
+    char *ws = static_cast<char *>(workspace);
+    float *part_o = sp.n_splits ? reinterpret_cast<float *>(ws + lay.part_o) : nullptr;
+    float *part_lse = sp.n_splits ? reinterpret_cast<float *>(ws + lay.part_lse) : nullptr;
+
+    if ((rc = mark(0)) != GR_OK) return rc;
+    if (sp.n_splits > 0) {
+        CtxArgs c;
+        c.g = g;
+        c.sp = sp;
+        c.q = static_cast<const uint16_t *>(q);
+        c.ctx_k = static_cast<const uint16_t *>(ctx_k);
+        c.ctx_v = static_cast<const uint16_t *>(ctx_v);
+        c.ctx_len = ctx_len;
+        c.part_o = part_o;
+        c.part_lse = part_lse;
+        c.err = dev.err_ptr;
+        rc = cuda_status(launch_ctx_simt(c, s));
+        if (rc != GR_OK) return rc;
+    }
+    if ((rc = mark(1)) != GR_OK) return rc;
+    MergeArgs m;
+    m.g = g;
+    m.n_splits = sp.n_splits;
+    m.q = static_cast<const uint16_t *>(q);
+    m.beam_k = static_cast<const uint16_t *>(beam_k);
+    m.beam_v = static_cast<const uint16_t *>(beam_v);
+    m.beam_path = beam_path;
+    m.part_o = part_o;
+    m.part_lse = part_lse;
+    m.out = static_cast<uint16_t *>(out);
+    m.lse = lse;
+    m.err = dev.err_ptr;
+    rc = cuda_status(launch_beam_merge(m, s));
+    if (rc != GR_OK) return rc;
+    return mark(2);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gr_decode_attn(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+                   const int32_t *ctx_len, const void *beam_k, const void *beam_v,
+                   const int32_t *beam_path, const int32_t *widths, int32_t step, void *out,
+                   float *lse, void *workspace, size_t workspace_bytes, gr_stream_t stream) {
+    return run_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
+                      lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *ctx_k,
+                         const void *ctx_v, const int32_t *ctx_len, const void *beam_k,
+                         const void *beam_v, const int32_t *beam_path, const int32_t *widths,
+                         int32_t step, void *out, float *lse, void *workspace,
+                         size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events) {
+    if (!events || !events[0] || !events[1] || !events[2]) return GR_ERR_NULL_ARG;
+    return run_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
+                      lse, workspace, workspace_bytes, stream, events);
+}
+
+int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32_t step,
+                        gr_plan_info *info) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!info) return GR_ERR_NULL_ARG;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    const SplitPlan sp = plan(g, dev.sm_count);
+    info->path = 1;
+    info->n_splits = sp.n_splits;
+    info->split_len = sp.split_len;
+    info->context_ctas = sp.n_splits ? ((g.W_s * g.G + 15) / 16) * g.R * g.Hkv * sp.n_splits : 0;
+    info->kernels = sp.n_splits ? 2 : 1;
+    info->fused_merge = 0;
+    return GR_OK;
+}
+
+int gr_resolve_ancestors(const gr_attn_shape *shape, const int32_t *beam_path, const int32_t *widths,
+                         int32_t step, int32_t *anc, gr_stream_t stream) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!beam_path || !anc) return GR_ERR_NULL_ARG;
+    if (misaligned(beam_path) || misaligned(anc)) return GR_ERR_MISALIGNED;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_ancestors(g, beam_path, anc, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_validate_beam_path(const gr_attn_shape *shape, const int32_t *beam_path, const int32_t *widths,
+                          int32_t step, const int32_t *ctx_len, int32_t *bad_count, gr_stream_t stream) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!beam_path || !ctx_len || !bad_count) return GR_ERR_NULL_ARG;
+    if (misaligned(beam_path) || misaligned(ctx_len)) return GR_ERR_MISALIGNED;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_validate(g, beam_path, ctx_len, bad_count, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_get_device_error(void) {
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GR_ERR_CUDA;
+    }
+    int code = 0;
+    if (cudaMemcpyFromSymbol(&code, g_device_error, sizeof code) != cudaSuccess) {
+        cudaGetLastError();
+        return GR_ERR_CUDA;
+    }
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) {
+        cudaGetLastError();
+        return GR_ERR_CUDA;
+    }
+    if (code == kDevErrTimeout) return GR_ERR_DEVICE_TIMEOUT;
+    if (code == kDevErrBadParent) return GR_ERR_BAD_BEAM_PATH;
+    return GR_OK;
+}
+
+}  // extern "C"

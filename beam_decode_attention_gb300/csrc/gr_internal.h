@@ -1,0 +1,70 @@
+// gr_internal.h -- launch parameters shared by the host front end and the
+// kernels of libgrattn.so (not installed; the public ABI is include/gr_attn.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gr {
+
+// Decode steps a call may name (widths travel to the kernels by value).
+constexpr int kMaxSteps = 64;
+
+// Bounded waits: a kernel that polls an mbarrier more often than this sets
+// the device error word and returns instead of hanging the GPU.
+constexpr long long kSpinLimit = 1LL << 25;
+
+// Device error codes written to the error word (first writer wins).
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrBadParent = 2;
+
+// Geometry of one call, resolved on the host.
+struct Geometry {
+    int R, Hq, Hkv, G, D;
+    int Lc_max, S_max, W_max;
+    int step, W_s;
+    float scale;        // softmax scale applied to q.k (natural-log units)
+    float scale_log2;   // softmax scale * log2(e)
+    int widths[kMaxSteps];
+};
+
+// Context-stage split of the key axis: split sp covers context positions
+// [sp * split_len, (sp + 1) * split_len) clipped to ctx_len[r].
+struct SplitPlan {
+    int n_splits;   // >= 1 when Lc_max > 0, 0 when there is no context
+    int split_len;  // multiple of the key-block size
+};
+
+struct CtxArgs {
+    Geometry g;
+    SplitPlan sp;
+    const uint16_t *q, *ctx_k, *ctx_v;
+    const int32_t *ctx_len;
+    float *part_o;    // fp32 [n_splits, R, W_s, Hq, D]  partial output, normalised
+    float *part_lse;  // fp32 [n_splits, R, W_s, Hq]     partial LSE (natural log)
+    int *err;
+};
+
+struct MergeArgs {
+    Geometry g;
+    int n_splits;
+    const uint16_t *q, *beam_k, *beam_v;
+    const int32_t *beam_path;
+    const float *part_o, *part_lse;
+    uint16_t *out;
+    float *lse;
+    int *err;
+};
+
+// gr_beam_merge.cu
+cudaError_t launch_beam_merge(const MergeArgs &a, cudaStream_t s);
+cudaError_t launch_ancestors(const Geometry &g, const int32_t *beam_path, int32_t *anc,
+                             cudaStream_t s);
+cudaError_t launch_validate(const Geometry &g, const int32_t *beam_path, const int32_t *ctx_len,
+                            int32_t *bad_count, cudaStream_t s);
+
+// gr_ctx_simt.cu  (CUDA-core context stage)
+cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
+
+}  // namespace gr

@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of gr_decode_attn on one GB300: µs per decode step and TFLOP/s
+at beam width 900 over a 2048-token context (Qwen3-0.6B attention heads,
+4 requests, 3 decode steps), with the roofline fraction of the dominant
+kernel, an end-to-end number through host buffers, and the CPU oracle timed
+on the host cores as a baseline.
+
+One bench step = the three decode-step calls (s = 0, 1, 2) of the workload;
+``value`` is the mean device time of one call (µs per decode step).  The L2
+is flushed (a 2x-L2 buffer is written) before every timed call; the flush
+is outside the timed interval.
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "µs/decode-step and TFLOP/s at BW=900, Lc=2048; % of bf16/HBM roofline"
+UNIT = "us/decode-step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_simt.cu"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOAD_BY_NAME))
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (what the method must do, not what a kernel happens to do)
+
+
+def chain_slots(inp, step):
+    """Distinct (step, slot) BeamKV entries the active beams reach, per request."""
+    bp, W = inp["beam_path"], inp["widths"]
+    out = []
+    for r in range(inp["num_requests"]):
+        cur = np.arange(int(W[step]))
+        n = len(cur)
+        for t in range(step, 0, -1):
+            cur = np.unique(bp[r, t, cur])
+            n += len(cur)
+        out.append(n)
+    return out
+
+
+def work(inp, step):
+    R, Hq, Hkv, D = inp["num_requests"], inp["num_q_heads"], inp["num_kv_heads"], inp["head_dim"]
+    W_s = int(inp["widths"][step])
+    lens = [int(x) for x in inp["ctx_len"]]
+    ctx_flops = 4.0 * W_s * Hq * D * sum(lens)
+    beam_flops = 4.0 * R * W_s * Hq * D * (step + 1)
+    ctx_bytes = float(sum(2 * Hkv * l * D * 2 for l in lens))
+    beam_bytes = float(sum(chain_slots(inp, step)) * Hkv * 2 * D * 2)
+    qo_bytes = 2.0 * R * W_s * Hq * D * 2
+    lse_bytes = 4.0 * R * W_s * Hq
+    path_bytes = 4.0 * R * sum(int(w) for w in inp["widths"][1:step + 1])
+    return dict(flops=ctx_flops + beam_flops, ctx_flops=ctx_flops,
+                bytes=ctx_bytes + beam_bytes + qo_bytes + lse_bytes + path_bytes,
+                ctx_bytes=ctx_bytes)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, only while the kernel source is unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_sha") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0], "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (the only place bench.py runs the oracle)
+
+
+def oracle_baseline(inp, seconds):
+    import oracle
+    orc = oracle.Oracle()
+    threads = orc.max_threads
+    R = inp["num_requests"]
+    total_rows = [R * int(w) for w in inp["widths"]]
+    # calibrate on a few rows of the last step, then size the sample
+    calib = [(r, b) for r in range(R) for b in range(0, int(inp["widths"][-1]), 97)][:max(threads, 8)]
+    t0 = time.perf_counter()
+    orc.decode_attn(inp, len(inp["widths"]) - 1, rows=calib)
+    per_row = (time.perf_counter() - t0) / len(calib)
+    est_full = per_row * sum(total_rows)
+    frac = min(1.0, seconds / max(est_full, 1e-9))
+    rng = np.random.default_rng(0)
+    spent, rows_done, per_step_us = 0.0, 0, []
+    for s, n in enumerate(total_rows):
+        W_s = int(inp["widths"][s])
+        k = max(1, int(round(n * frac)))
+        flat = rng.choice(n, size=k, replace=False) if k < n else np.arange(n)
+        rows = [(int(i // W_s), int(i % W_s)) for i in flat]
+        t0 = time.perf_counter()
+        orc.decode_attn(inp, s, rows=None if k == n else rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        rows_done += k
+        per_step_us.append(dt / k * n * 1e6)
+    value = float(np.mean(per_step_us))
+    sample = (f"{rows_done} of {sum(total_rows)} (request, beam) rows over the 3 decode steps "
+              f"({100 * rows_done / sum(total_rows):.1f}%), every head; time scaled to whole steps"
+              if frac < 1.0 else "every row of the 3 decode steps")
+    return dict(value=value, unit=UNIT, cores=threads, kind="oracle", sample=sample,
+                cpu_seconds=spent)
+
+
+# ----------------------------------------------------------------------------
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    spec = workloads.WORKLOAD_BY_NAME[args.workload]
+    inp = workloads.make_inputs(spec)
+    per_step = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        b = oracle_baseline(inp, per_step)
+        if i >= args.warmup:
+            vals.append(b["value"])
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value * 3 / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(spec, inp),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": b["cores"], "kind": "oracle",
+                         "sample": b["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(spec, inp):
+    return {"workload": spec.name, "requests": spec.num_requests, "q_heads": spec.num_q_heads,
+            "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "ctx_len": [int(x) for x in inp["ctx_len"]] if spec.lc_range else spec.lc,
+            "beam_widths": list(spec.widths), "decode_steps": spec.steps,
+            "l2": "flushed (2x L2 buffer written) before every timed call"}
+
+
+def main():
+    args = parse_args()
+    if args.gpus != 1:
+        print(json.dumps({"error": "this build runs on one GPU; --gpus must be 1"}))
+        return 2
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import beam_decode_attention_gb300 as gr
+
+    torch.cuda.set_device(0)
+    spec = workloads.WORKLOAD_BY_NAME[args.workload]
+    inp = workloads.make_inputs(spec)
+    S = spec.steps
+    dev = torch.device("cuda:0")
+
+    def up(a):
+        a = a.view(np.int16) if a.dtype == np.uint16 else a
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    shape = gr.Shape.of(inp)
+    widths = [int(w) for w in inp["widths"]]
+    ctx_k, ctx_v, ctx_len = up(inp["ctx_k"]), up(inp["ctx_v"]), up(inp["ctx_len"])
+    beam_k, beam_v, beam_path = up(inp["beam_k"]), up(inp["beam_v"]), up(inp["beam_path"])
+    qs = [up(x) for x in inp["q"]]
+    R, Hq, D = spec.num_requests, spec.num_q_heads, spec.head_dim
+    outs = [torch.empty(R * widths[s] * Hq * D, dtype=torch.int16, device=dev) for s in range(S)]
+    lses = [torch.empty(R * widths[s] * Hq, dtype=torch.float32, device=dev) for s in range(S)]
+    ws_bytes = max(gr.gr_decode_attn_workspace_size(shape, widths, s) for s in range(S))
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    plans = [gr.gr_decode_attn_plan(shape, widths, s) for s in range(S)]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    works = [work(inp, s) for s in range(S)]
+
+    def call(s, ev=None):
+        if ev is None:
+            gr.gr_decode_attn(shape, qs[s], ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, s,
+                              outs[s], lses[s], ws, stream=stream)
+        else:
+            gr.gr_decode_attn_timed(shape, qs[s], ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
+                                    widths, s, outs[s], lses[s], ws, ev, stream=stream)
+
+    for _ in range(args.warmup):
+        for s in range(S):
+            flush.zero_()
+            call(s)
+    torch.cuda.synchronize()
+    if gr.gr_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(S)]
+              for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        for s in range(S):
+            flush.zero_()
+            call(s, events[k][s])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if gr.gr_get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    call_ms = [[events[k][s][0].elapsed_time(events[k][s][2]) for s in range(S)] for k in range(args.steps)]
+    ctx_ms = [[events[k][s][0].elapsed_time(events[k][s][1]) for s in range(S)] for k in range(args.steps)]
+    per_step_us = [1000.0 * float(np.mean([call_ms[k][s] for k in range(args.steps)])) for s in range(S)]
+    per_step_ctx_us = [1000.0 * float(np.mean([ctx_ms[k][s] for k in range(args.steps)])) for s in range(S)]
+    value = float(np.mean(per_step_us))
+    total_flops = sum(w["flops"] for w in works)
+    tflops = total_flops / (sum(per_step_us) * 1e-6) / 1e12
+
+    pk = peaks()
+    # dominant kernel: the context stage; its algorithmic FLOPs per launch are
+    # 4 * W_s * Hq * D * sum(ctx_len), the same for each step's launch
+    ctx_flops = sum(w["ctx_flops"] for w in works)
+    ctx_time = sum(per_step_ctx_us) * 1e-6
+    achieved_tf = ctx_flops / ctx_time / 1e12
+    traffic = recorded_traffic(spec.name)
+    roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved_tf / pk["bf16_tflops"], 4),
+                "traffic": traffic, "kernel": "context stage",
+                "peak_source": f"{pk['source']} bf16 burst"}
+    roof_us = [max(w["flops"] / (pk["bf16_tflops"] * 1e12), w["bytes"] / (pk["hbm_gbs"] * 1e9)) * 1e6
+               for w in works]
+    call_roofline = {"roofline_us_per_step": [round(x, 2) for x in roof_us],
+                     "measured_us_per_step": [round(x, 2) for x in per_step_us],
+                     "frac_per_step": [round(a / b, 4) for a, b in zip(roof_us, per_step_us)],
+                     "frac": round(sum(roof_us) / sum(per_step_us), 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(gr, torch, inp, shape, widths, ws, stream, args)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_baseline(inp, args.cpu_seconds)
+
+    launches = sum(p["kernels"] for p in plans) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sum(per_step_us) / 1000.0, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(spec, inp),
+        "tflops": round(tflops, 2), "us_per_decode_step": [round(x, 2) for x in per_step_us],
+        "context_kernel_us": [round(x, 2) for x in per_step_ctx_us],
+        "roofline": roofline, "call_roofline": call_roofline,
+        "plan": plans, "gpu_launches": launches, "clocks": clk,
+        "cpu_baseline": cpu, "e2e": e2e,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def end_to_end(gr, torch, inp, shape, widths, ws, stream, args):
+    """The same calls from pinned host buffers: each call's inputs are copied
+    host->device, the call runs, out and lse come back device->host."""
+    S = len(widths)
+    R, Hq, D = inp["num_requests"], inp["num_q_heads"], inp["head_dim"]
+
+    def pin(a):
+        a = a.view(np.int16) if a.dtype == np.uint16 else a
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    host = {k: pin(inp[k]) for k in ("ctx_k", "ctx_v", "ctx_len", "beam_k", "beam_v", "beam_path")}
+    host_q = [pin(x) for x in inp["q"]]
+    devb = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    dev_q = [torch.empty_like(x, device="cuda") for x in host_q]
+    outs = [torch.empty(R * widths[s] * Hq * D, dtype=torch.int16, device="cuda") for s in range(S)]
+    lses = [torch.empty(R * widths[s] * Hq, dtype=torch.float32, device="cuda") for s in range(S)]
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    host_lse = [torch.empty_like(x, device="cpu").pin_memory() for x in lses]
+    h2d = [sum(v.numel() * v.element_size() for v in host.values()) + host_q[s].numel() * 2
+           for s in range(S)]
+    d2h = [outs[s].numel() * 2 + lses[s].numel() * 4 for s in range(S)]
+
+    def one(s):
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        dev_q[s].copy_(host_q[s], non_blocking=True)
+        gr.gr_decode_attn(shape, dev_q[s], devb["ctx_k"], devb["ctx_v"], devb["ctx_len"],
+                          devb["beam_k"], devb["beam_v"], devb["beam_path"], widths, s, outs[s],
+                          lses[s], ws, stream=stream)
+        host_out[s].copy_(outs[s], non_blocking=True)
+        host_lse[s].copy_(lses[s], non_blocking=True)
+
+    for _ in range(args.warmup):
+        for s in range(S):
+            one(s)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        for s in range(S):
+            one(s)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / (steps * S)
+    return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": int(np.mean(h2d)),
+            "d2h_bytes_per_step": int(np.mean(d2h)),
+            "note": "per decode-step call: every input the call reads copied from pinned host memory"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

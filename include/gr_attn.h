@@ -1,0 +1,189 @@
+/*
+ * gr_attn.h -- C ABI of libgrattn.so: large-beam decode attention over a
+ * shared request context (ContextKV + BeamKV + BeamPath), for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation (GR-Inference blog, "system design" and "kernel design";
+ * SID-GR Inference README, section 3 "Design Highlights" and section 9
+ * "Nsight breakdown"; xGR review, "xAttention", three-stage computation):
+ *
+ *   For request r, active beam b < W_s at decode step s and query head h
+ *   (kv head g = h / G, G = Hq / Hkv), with the ancestor chain
+ *       a_s = b,   a_{t-1} = beam_path[r, t, a_t]   (t = s .. 1)
+ *   the row attends to the keys/values
+ *       ctx_k/ctx_v[r, g, 0 .. ctx_len[r]-1]             (shared stage)
+ *       beam_k/beam_v[r, t, a_t, g]  for t = 0 .. s      (unshared stage)
+ *   with scores x_j = softmax_scale * <q[r, b, h], k_j>, and the two partial
+ *   softmaxes are merged exactly by log-sum-exp (merging stage):
+ *       lse[r, b, h] = ln sum_j exp(x_j)
+ *       out[r, b, h] = sum_j exp(x_j - lse) * v_j
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller allocates and owns every buffer.  No entry point
+ *     here allocates or frees memory, and only gr_get_device_error()
+ *     synchronises.
+ *   - Execution: device work is enqueued on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and runs asynchronously.  Host-side checks
+ *     happen before anything is enqueued; on an error nothing is enqueued.
+ *   - Layout: every tensor is dense, row-major, with the shapes below.  bf16
+ *     is IEEE bfloat16 stored in 2 bytes.  Device pointers must be 16-byte
+ *     aligned.
+ *   - Widths are per step and shared by every request in the call
+ *     (`widths` is a HOST array of at least step+1 entries).
+ *   - The caller appends the step-s K/V of every active beam to beam_k/beam_v
+ *     before the call, so each chain holds s+1 tokens (the current token is
+ *     attended).
+ *   - Preconditions not checked on the hot path (gr_validate_beam_path checks
+ *     them on the device): 0 <= ctx_len[r] <= ctx_capacity; beam_path[r, t, b]
+ *     in [0, widths[t-1]) for 1 <= t <= s and b < widths[t].  beam_path[r, 0, .]
+ *     is never read (step 0 expands from the single prefill row).
+ *   - Returns GR_OK (0) or a negative gr_status.
+ */
+#ifndef GR_ATTN_H
+#define GR_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *gr_stream_t; /* a cudaStream_t */
+typedef void *gr_event_t;  /* a cudaEvent_t */
+
+typedef enum {
+    GR_OK = 0,
+    GR_ERR_NULL_ARG = -1,            /* a required pointer is NULL */
+    GR_ERR_BAD_SHAPE = -2,           /* inconsistent or out-of-range sizes */
+    GR_ERR_UNSUPPORTED = -3,         /* head_dim not 64/128, or no sm_103 device */
+    GR_ERR_MISALIGNED = -4,          /* a device pointer is not 16-byte aligned */
+    GR_ERR_WORKSPACE_TOO_SMALL = -5, /* workspace_bytes below the size required */
+    GR_ERR_CUDA = -6,                /* a CUDA runtime/driver call failed */
+    GR_ERR_DEVICE_TIMEOUT = -7,      /* a kernel gave up a bounded wait */
+    GR_ERR_BAD_BEAM_PATH = -8        /* a kernel met a parent slot out of range */
+} gr_status;
+
+/* Problem geometry.  Every size is a count of elements, not bytes. */
+typedef struct {
+    int32_t num_requests;  /* R >= 1 */
+    int32_t num_q_heads;   /* Hq >= 1 */
+    int32_t num_kv_heads;  /* Hkv >= 1, Hq % Hkv == 0, G = Hq / Hkv <= 128 */
+    int32_t head_dim;      /* D: 64 or 128 */
+    int32_t ctx_capacity;  /* Lc_max >= 0: context slots per (request, kv head) */
+    int32_t step_capacity; /* S_max >= 1: decode-step slots in BeamKV/BeamPath */
+    int32_t beam_capacity; /* W_max >= 1: beam slots per step */
+    float softmax_scale;   /* score scale (1/sqrt(D) for the Qwen3 heads) */
+} gr_attn_shape;
+
+/*
+ * Bytes of device workspace gr_decode_attn needs for this geometry, step and
+ * width schedule (host array, step+1 entries).  Depends only on the shape,
+ * widths[step] and the device's SM count; 0 on a bad argument.
+ */
+size_t gr_decode_attn_workspace_size(const gr_attn_shape *shape, const int32_t *widths,
+                                     int32_t step);
+
+/*
+ * Decode attention for all requests at decode step `step`.
+ *
+ *   q          device bf16 [R, W_s, Hq, D]          W_s = widths[step]
+ *   ctx_k      device bf16 [R, Hkv, Lc_max, D]      shared ContextKV
+ *   ctx_v      device bf16 [R, Hkv, Lc_max, D]
+ *   ctx_len    device int32 [R]                     valid context positions
+ *   beam_k     device bf16 [R, S_max, W_max, Hkv, D] BeamKV
+ *   beam_v     device bf16 [R, S_max, W_max, Hkv, D]
+ *   beam_path  device int32 [R, S_max, W_max]       parent slot at step t-1
+ *   widths     HOST int32 [step+1]                  active width per step
+ *   out        device bf16 [R, W_s, Hq, D]          written (round to nearest even)
+ *   lse        device fp32 [R, W_s, Hq]             written, natural log of the
+ *                                                   summed exp of scaled scores
+ *   workspace  device scratch of workspace_bytes >= gr_decode_attn_workspace_size()
+ *              (16-byte aligned; may be NULL when that size is 0)
+ *
+ * Context positions >= ctx_len[r] are never used, whatever they hold.
+ * Errors: GR_ERR_NULL_ARG, GR_ERR_BAD_SHAPE (step outside [0, S_max),
+ * widths[t] outside [1, W_max], ...), GR_ERR_UNSUPPORTED, GR_ERR_MISALIGNED,
+ * GR_ERR_WORKSPACE_TOO_SMALL, GR_ERR_CUDA (launch failure).
+ */
+int gr_decode_attn(const gr_attn_shape *shape, const void *q, const void *ctx_k,
+                   const void *ctx_v, const int32_t *ctx_len, const void *beam_k,
+                   const void *beam_v, const int32_t *beam_path, const int32_t *widths,
+                   int32_t step, void *out, float *lse, void *workspace,
+                   size_t workspace_bytes, gr_stream_t stream);
+
+/*
+ * gr_decode_attn, plus three CUDA events recorded on `stream`: events[0]
+ * before the context-stage kernel, events[1] after it (before the per-beam
+ * stage and merge), events[2] after the last kernel.  Elapsed times between
+ * them give each kernel's device time without a profiler.  `events` is a
+ * HOST array of 3 created events (cudaEventCreate); all other arguments and
+ * errors are those of gr_decode_attn.
+ */
+int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *ctx_k,
+                         const void *ctx_v, const int32_t *ctx_len, const void *beam_k,
+                         const void *beam_v, const int32_t *beam_path, const int32_t *widths,
+                         int32_t step, void *out, float *lse, void *workspace,
+                         size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events);
+
+/* How gr_decode_attn will run a given call (filled by gr_decode_attn_plan). */
+typedef struct {
+    int32_t path;            /* 0: tensor-core context stage, 1: CUDA-core context stage */
+    int32_t n_splits;        /* key splits of the context stage (0: no context) */
+    int32_t split_len;       /* context positions per split */
+    int32_t context_ctas;    /* CTAs of the context-stage kernel */
+    int32_t kernels;         /* kernels one call launches */
+    int32_t fused_merge;     /* 1 when the context kernel also runs the per-beam stage and merge */
+} gr_plan_info;
+
+/*
+ * Fills *info with the plan gr_decode_attn would use for this geometry and
+ * step on the current device.  Errors: those of the shape checks, and
+ * GR_ERR_CUDA / GR_ERR_UNSUPPORTED when no sm_103 device is current.
+ */
+int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32_t step,
+                        gr_plan_info *info);
+
+/*
+ * The ancestor walk alone (BeamPath parent pointers, GR-Inference blog
+ * "system design"): anc[r, b, t] = a_t for b < widths[step], t = 0 .. step.
+ *   anc  device int32 [R, W_s, step+1], written.
+ * For debugging and tests; the same walk runs inside gr_decode_attn.  An
+ * out-of-range parent is not followed: the walk stops there and writes -1
+ * for it and for every earlier step.
+ */
+int gr_resolve_ancestors(const gr_attn_shape *shape, const int32_t *beam_path,
+                         const int32_t *widths, int32_t step, int32_t *anc,
+                         gr_stream_t stream);
+
+/*
+ * Checks gr_decode_attn's unchecked preconditions on the device: counts
+ * parents outside [0, widths[t-1]) (1 <= t <= step, b < widths[t]) and
+ * ctx_len entries outside [0, Lc_max].  *bad_count (device int32) is
+ * overwritten with the count.  Reads nothing out of range itself.
+ */
+int gr_validate_beam_path(const gr_attn_shape *shape, const int32_t *beam_path,
+                          const int32_t *widths, int32_t step, const int32_t *ctx_len,
+                          int32_t *bad_count, gr_stream_t stream);
+
+/*
+ * Synchronises the current device, then returns and clears the library's
+ * device error word: GR_OK; GR_ERR_DEVICE_TIMEOUT when a kernel gave up a
+ * bounded wait (its outputs are then incomplete); GR_ERR_BAD_BEAM_PATH when
+ * gr_decode_attn met a BeamPath parent outside [0, widths[t-1]) (it reads
+ * nothing out of range and writes NaN to the affected rows).  GR_ERR_CUDA
+ * when the synchronisation itself fails.
+ */
+int gr_get_device_error(void);
+
+/* Static description of a gr_status code. */
+const char *gr_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GR_ATTN_H */

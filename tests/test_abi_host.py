@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/gr_attn.h declares, and rejects bad arguments before
+touching a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import beam_decode_attention_gb300 as gr
+from beam_decode_attention_gb300 import build as gr_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gr_build.build()
+    return gr.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gr_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gr_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "gr_decode_attn" in names and "gr_resolve_ancestors" in names
+    assert set(names) == set(gr.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert gr.gr_status_string(0) == "ok"
+    for code in range(-8, 0):
+        assert gr.gr_status_string(code) != "unknown status"
+    assert gr.gr_status_string(-99) == "unknown status"
+    assert gr.gr_version() >= 100
+
+
+def _shape(**kw):
+    d = dict(num_requests=2, num_q_heads=16, num_kv_heads=8, head_dim=128, ctx_capacity=64,
+             step_capacity=3, beam_capacity=8, softmax_scale=0.088388)
+    d.update(kw)
+    return gr.Shape.of(d)
+
+
+FAKE = 1 << 20   # a 16-byte-aligned address that is never dereferenced
+
+
+def _call(shape, widths=(4, 4, 4), step=2, **ptrs):
+    lib = gr.load()
+    p = dict(q=FAKE, ck=FAKE, cv=FAKE, cl=FAKE, bk=FAKE, bv=FAKE, bp=FAKE, out=FAKE, lse=FAKE, ws=FAKE)
+    p.update(ptrs)
+    w = (ctypes.c_int32 * len(widths))(*widths)
+    return lib.gr_decode_attn(ctypes.byref(shape), p["q"], p["ck"], p["cv"], p["cl"], p["bk"],
+                              p["bv"], p["bp"], w, step, p["out"], p["lse"], p["ws"], 1 << 30, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_requests=0), -2),
+    (dict(num_q_heads=12, num_kv_heads=8), -2),
+    (dict(head_dim=96), -3),
+    (dict(num_q_heads=256, num_kv_heads=1), -3),
+    (dict(step_capacity=0), -2),
+    (dict(beam_capacity=0), -2),
+    (dict(ctx_capacity=-1), -2),
+    (dict(softmax_scale=float("nan")), -2),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    assert _call(_shape(**kw)) == code
+
+
+def test_bad_step_and_widths_rejected(lib):
+    assert _call(_shape(), step=3) == -2
+    assert _call(_shape(), step=-1) == -2
+    assert _call(_shape(), widths=(4, 9, 4)) == -2       # > beam_capacity
+    assert _call(_shape(), widths=(4, 0, 4)) == -2
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    assert _call(_shape(), q=None) == -1
+    assert _call(_shape(), out=None) == -1
+    assert _call(_shape(), bp=None) == -1
+    assert _call(_shape(), ck=None) == -1
+    assert _call(_shape(), q=FAKE + 8) == -4
+    assert _call(_shape(), lse=FAKE + 4) == -4
+    assert _call(_shape(), ws=FAKE + 2) == -4
+
+
+def test_workspace_size_zero_on_bad_args(lib):
+    w = (ctypes.c_int32 * 3)(4, 4, 4)
+    assert lib.gr_decode_attn_workspace_size(ctypes.byref(_shape(head_dim=80)), w, 2) == 0
+    assert lib.gr_decode_attn_workspace_size(None, w, 2) == 0
+    assert lib.gr_decode_attn_workspace_size(ctypes.byref(_shape()), w, 5) == 0
+
+
+def test_utilities_reject_bad_args(lib):
+    w = (ctypes.c_int32 * 3)(4, 4, 4)
+    assert lib.gr_resolve_ancestors(ctypes.byref(_shape()), None, w, 2, FAKE, 0) == -1
+    assert lib.gr_resolve_ancestors(ctypes.byref(_shape()), FAKE, w, 7, FAKE, 0) == -2
+    assert lib.gr_validate_beam_path(ctypes.byref(_shape()), FAKE, w, 2, None, FAKE, 0) == -1

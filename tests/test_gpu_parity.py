@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Gate (stated with the target): BeamPath handling bit-exact; max |out - oracle|
+<= 1e-2 on the bf16 outputs; max |lse - oracle| <= 1e-3.  The oracle is fp64;
+the CUDA path computes in fp32 with bf16 P on the tensor cores.
+"""
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():   # pragma: no cover - CPU-only machines
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from gpu_util import DeviceWorkload, compare  # noqa: E402
+
+ORC = oracle.Oracle()
+_CACHE = {}
+
+
+def workload(name):
+    if name not in _CACHE:
+        inp = workloads.make_inputs(workloads.WORKLOAD_BY_NAME[name])
+        _CACHE[name] = (inp, DeviceWorkload(inp))
+    return _CACHE[name]
+
+
+def sample_rows(inp, step, n_random=40, seed=0):
+    """Rows the oracle recomputes one by one at full size: the first and last
+    beams of every request, beams on either side of 128-row tile edges, and
+    random beams."""
+    R, W_s, G = inp["num_requests"], int(inp["widths"][step]), inp["num_q_heads"] // inp["num_kv_heads"]
+    per_tile = max(1, 128 // G)
+    rows = set()
+    for r in range(R):
+        for b in (0, W_s - 1, per_tile - 1, per_tile, 2 * per_tile - 1, 2 * per_tile):
+            if 0 <= b < W_s:
+                rows.add((r, b))
+    rng = np.random.default_rng(seed + step)
+    for _ in range(n_random):
+        rows.add((int(rng.integers(R)), int(rng.integers(W_s))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", [workloads.WORKLOADS[0].name, workloads.WORKLOADS[1].name])
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_small_workloads_every_row(name, step):
+    inp, dev = workload(name)
+    out, lse = dev.run(step, guard=64)
+    ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+    compare(out, lse, ref_out, ref_lse)
+    assert np.array_equal(dev.ancestors(step), ref_anc)
+
+
+@pytest.mark.parametrize("name", [w.name for w in workloads.WORKLOADS[2:]])
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_full_size_sampled_rows(name, step):
+    inp, dev = workload(name)
+    out, lse = dev.run(step, guard=64)
+    # every row: finite, and bounded by the largest |value| it could average
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    vmax = max(float(np.nanmax(np.abs(workloads.bf16_bits_to_f32(inp["ctx_v"])))),
+               float(np.nanmax(np.abs(workloads.bf16_bits_to_f32(inp["beam_v"])))))
+    assert float(np.max(np.abs(out))) <= vmax * (1 + 2 ** -7)
+    rows = sample_rows(inp, step)
+    ref_out, ref_lse, _ = ORC.decode_attn(inp, step, rows=rows)
+    idx_r = np.array([r for r, _ in rows])
+    idx_b = np.array([b for _, b in rows])
+    compare(out[idx_r, idx_b], lse[idx_r, idx_b], ref_out, ref_lse)
+    # BeamPath: bit-exact on every row
+    assert np.array_equal(dev.ancestors(step), ORC.ancestors(inp, step))
+
+
+def _run_custom(inp, steps=None, splits=None):
+    dev = DeviceWorkload(inp)
+    for step in (steps if steps is not None else range(len(inp["widths"]))):
+        if splits is not None:
+            os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+        try:
+            out, lse = dev.run(step, guard=32)
+        finally:
+            os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+        ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+        compare(out, lse, ref_out, ref_lse)
+        assert np.array_equal(dev.ancestors(step), ref_anc)
+
+
+def test_multi_tile_ragged():
+    """Several 128-row tiles per (request, kv head) with a ragged last tile,
+    several key blocks, ragged context lengths."""
+    inp = workloads.make_custom(3, 16, 8, 128, [300, 1000, 129], [5, 70, 133], seed=101)
+    _run_custom(inp)
+
+
+@pytest.mark.parametrize("lens", [[0, 0], [1, 7], [127, 128], [129, 255], [0, 256]])
+def test_context_length_edges(lens):
+    inp = workloads.make_custom(2, 16, 8, 128, lens, [3, 9, 65], seed=sum(lens) + 3, lc_max=300)
+    _run_custom(inp)
+
+
+def test_no_context_capacity():
+    inp = workloads.make_custom(2, 4, 2, 64, [0, 0], [2, 3, 4], seed=5, lc_max=0)
+    _run_custom(inp)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 128), (16, 4, 128), (32, 4, 64), (4, 2, 64), (12, 4, 128)])
+def test_head_geometries(Hq, Hkv, D):
+    inp = workloads.make_custom(2, Hq, Hkv, D, [200, 77], [7, 33, 50], seed=Hq * 7 + Hkv + D)
+    _run_custom(inp)
+
+
+def test_width_one():
+    inp = workloads.make_custom(3, 16, 8, 128, [64, 500, 3], [1, 1, 1], seed=17)
+    _run_custom(inp)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_splits(splits):
+    inp = workloads.make_custom(2, 16, 8, 128, [777, 1024], [16, 40, 72], seed=29)
+    _run_custom(inp, steps=[2], splits=splits)
+
+
+def test_tagged_beam_values():
+    """Context V = 0, each beam token's V is a one-hot code of (step, slot),
+    queries sharpened x4: out names the chain tokens and their weights, so a
+    wrong ancestor or a missing beam term gives an O(0.1) error."""
+    D = 128
+    inp = workloads.make_custom(2, 16, 8, D, [40, 300], [5, 9, 12], seed=61, q_scale=4.0)
+    inp["ctx_v"][:] = 0
+    W_max = inp["beam_capacity"]
+    for t in range(3):
+        for a in range(W_max):
+            inp["beam_v"][:, t, a] = 0
+            inp["beam_v"][:, t, a, :, t * W_max + a] = 0x3F80
+    dev = DeviceWorkload(inp)
+    for step in range(3):
+        out, lse = dev.run(step)
+        ref_out, ref_lse, _ = ORC.decode_attn(inp, step)
+        assert float(np.max(np.abs(ref_out))) > 0.2
+        compare(out, lse, ref_out, ref_lse)
+
+
+def test_repeatable_and_stream():
+    inp = workloads.make_custom(2, 16, 8, 128, [333, 64], [8, 20, 30], seed=71)
+    dev = DeviceWorkload(inp)
+    a = dev.run(2)
+    s = torch.cuda.Stream()
+    b = dev.run(2, stream=s)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_bad_parent_is_reported_not_followed():
+    """A parent outside [0, W_{t-1}) is counted by gr_validate_beam_path; the
+    decode call reads nothing out of range, writes NaN to the rows whose
+    chain meets it, flags the device error word, and leaves the other rows
+    right."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(2, 4, 2, 64, [10, 20], [3, 4, 5], seed=83)
+    inp["beam_path"][1, 2, 2] = 4            # widths[1] == 4: out of range
+    inp["beam_path"][0, 1, 0] = -3
+    dev = DeviceWorkload(inp)
+    assert gr.gr_get_device_error() == 0
+    bad = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gr.gr_validate_beam_path(dev.shape, dev.beam_path, dev.widths, 2, dev.ctx_len, bad)
+    torch.cuda.synchronize()
+    assert int(bad.item()) == 2
+    out, lse = dev.run(2)
+    assert gr.gr_get_device_error() == -8    # GR_ERR_BAD_BEAM_PATH
+    assert gr.gr_get_device_error() == 0     # reading clears the word
+
+    def hits_bad(r, b):
+        slot = b
+        for t in (2, 1):
+            p = int(inp["beam_path"][r, t, slot])
+            if not 0 <= p < int(inp["widths"][t - 1]):
+                return True
+            slot = p
+        return False
+
+    affected = [(r, b) for r in range(2) for b in range(5) if hits_bad(r, b)]
+    good = [(r, b) for r in range(2) for b in range(5) if not hits_bad(r, b)]
+    assert (1, 2) in affected and good
+    for r, b in affected:
+        assert np.isnan(out[r, b]).all() and np.isnan(lse[r, b]).all()
+    anc = dev.ancestors(2)
+    assert list(anc[1, 2]) == [-1, -1, 2]
+    fixed = dict(inp, beam_path=np.where((inp["beam_path"] == 4) | (inp["beam_path"] == -3), 0,
+                                         inp["beam_path"]))
+    ref_out, ref_lse, _ = ORC.decode_attn(fixed, 2, rows=good)
+    idx_r = np.array([r for r, _ in good]); idx_b = np.array([b for _, b in good])
+    compare(out[idx_r, idx_b], lse[idx_r, idx_b], ref_out, ref_lse)
+
+
+def test_error_statuses():
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(1, 4, 2, 64, [10], [2, 2], seed=3)
+    dev = DeviceWorkload(inp)
+    out, lse = dev.outputs(1)
+    need = gr.gr_decode_attn_workspace_size(dev.shape, dev.widths, 1)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gr.GRError) as e:
+        gr.gr_decode_attn(dev.shape, dev.q[1], dev.ctx_k, dev.ctx_v, dev.ctx_len, dev.beam_k,
+                          dev.beam_v, dev.beam_path, dev.widths, 1, out, lse, small)
+    assert e.value.status == -5
+    big = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gr.GRError) as e:
+        gr.gr_decode_attn(dev.shape, dev.q[1], dev.ctx_k, dev.ctx_v, dev.ctx_len, dev.beam_k,
+                          dev.beam_v, dev.beam_path, dev.widths, 1, out[1:], lse, big)
+    assert e.value.status == -4
+    with pytest.raises(gr.GRError) as e:
+        gr.gr_decode_attn(dev.shape, dev.q[1], dev.ctx_k, dev.ctx_v, dev.ctx_len, dev.beam_k,
+                          dev.beam_v, dev.beam_path, [2, 3], 1, out, lse, big)
+    assert e.value.status == -2
