@@ -27,13 +27,17 @@ __all__ = [
     "GRError", "Shape", "load", "lib_path", "gr_decode_attn", "gr_decode_attn_workspace_size",
     "gr_resolve_ancestors", "gr_validate_beam_path", "gr_get_device_error", "gr_status_string",
     "gr_version", "EXPORTED_SYMBOLS", "gr_decode_attn_timed", "gr_decode_attn_plan", "PlanInfo",
+    "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 EXPORTED_SYMBOLS = (
     "gr_decode_attn_workspace_size", "gr_decode_attn", "gr_decode_attn_timed",
     "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
-    "gr_get_device_error", "gr_status_string", "gr_version",
+    "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
 )
+
+# bytes of the library's static scratch used by gr_decode_attn_noalloc
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 GR_OK = 0
 STATUS_NAMES = {
@@ -112,6 +116,8 @@ def load() -> ctypes.CDLL:
     lib.gr_decode_attn_timed.restype = ctypes.c_int
     lib.gr_decode_attn_plan.argtypes = [sp, vp, i32, ctypes.POINTER(PlanInfo)]
     lib.gr_decode_attn_plan.restype = ctypes.c_int
+    lib.gr_decode_attn_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+    lib.gr_decode_attn_noalloc.restype = ctypes.c_int
     lib.gr_resolve_ancestors.argtypes = [sp, vp, vp, i32, vp, vp]
     lib.gr_resolve_ancestors.restype = ctypes.c_int
     lib.gr_validate_beam_path.argtypes = [sp, vp, vp, i32, vp, vp, vp]
@@ -201,6 +207,20 @@ def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v,
                                      int(step), _ptr(out), _ptr(lse), _ptr(workspace),
                                      int(workspace_bytes), _stream_handle(stream), ev)
     _check(rc, "gr_decode_attn_timed")
+
+
+def gr_decode_attn_noalloc(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
+                           widths: Sequence[int], step: int, out, lse, stream=None) -> None:
+    """gr_decode_attn without a caller-supplied workspace: for callers that
+    cannot allocate device memory, the library uses its own static 64 MiB
+    device scratch (shared by all calls; calls that overlap on the GPU race).
+    Raises :class:`GRError` (GR_ERR_WORKSPACE_TOO_SMALL) when the call needs
+    more scratch than that."""
+    rc = load().gr_decode_attn_noalloc(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
+                                       _ptr(ctx_len), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path),
+                                       _widths_arr(widths), int(step), _ptr(out), _ptr(lse),
+                                       _stream_handle(stream))
+    _check(rc, "gr_decode_attn_noalloc")
 
 
 def gr_decode_attn_plan(shape: Shape, widths: Sequence[int], step: int) -> dict:

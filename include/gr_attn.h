@@ -113,6 +113,44 @@ int gr_decode_attn(const gr_attn_shape *shape, const void *q, const void *ctx_k,
                    size_t workspace_bytes, gr_stream_t stream);
 
 /*
+ * Size of the static device scratch gr_decode_attn_noalloc uses: 64 MiB.
+ */
+#define GR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * gr_decode_attn for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for callers such as
+ * code running in a host callback enqueued on a stream (where CUDA calls
+ * that allocate are not allowed), code inside an engine whose memory pool
+ * already holds the device memory (so another cudaMalloc fails or breaks its
+ * accounting), and latency-critical paths that cannot pay for cudaMalloc's
+ * implicit synchronisation.
+ *
+ * Same arguments, results and errors as gr_decode_attn, without the
+ * workspace: the partial results live in a static device array of
+ * GR_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU that loads the
+ * library holds that array until the process exits.  The caller still
+ * passes every input and output buffer.  This entry point allocates and
+ * frees nothing.
+ *
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - A call whose plan needs more scratch than GR_NOALLOC_SCRATCH_BYTES
+ *     (gr_decode_attn_workspace_size() larger than it) returns
+ *     GR_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs clearing, since each call writes every scratch
+ *     entry before reading it.  Calls that may overlap on the GPU (on
+ *     different streams, or from several host threads) race on the array:
+ *     order them on one stream or with events.
+ */
+int gr_decode_attn_noalloc(const gr_attn_shape *shape, const void *q, const void *ctx_k,
+                           const void *ctx_v, const int32_t *ctx_len, const void *beam_k,
+                           const void *beam_v, const int32_t *beam_path, const int32_t *widths,
+                           int32_t step, void *out, float *lse, gr_stream_t stream);
+
+/*
  * gr_decode_attn, plus three CUDA events recorded on `stream`: events[0]
  * before the context-stage kernel, events[1] after it (before the per-beam
  * stage and merge), events[2] after the last kernel.  Elapsed times between
