@@ -1,0 +1,483 @@
+// gr_ctx_tc.cu -- shared (context) stage on the fifth-generation tensor cores.
+//
+// The shared stage is the one dense contraction of this attention: every
+// query row (active beam x query head) of a request / kv-head pair attends to
+// the same ContextKV, so the W*G rows of the pair form one dense M dimension
+// and the context is streamed once per 256 rows instead of once per beam
+// (GR-Inference blog, "kernel design": tensor-core MMA with split-KV over the
+// long ContextKV; SID-GR README, section 9: the context part is processed per
+// request and beam tile).  Online softmax over 128-key blocks follows the
+// FlashAttention-style blocking the xGR review describes ("xAttention").
+//
+// One CTA = one (request, kv head, pair of 128-row tiles, key split):
+//   warp 8      TMA producer: Q tiles once, then K/V blocks through a
+//               4-slot shared-memory ring (128-byte swizzle).
+//   warp 9      tensor-core issuer (one lane): S_t = Q_t K^T into TMEM,
+//               O_t += P_t V with P read back from TMEM; owns the TMEM.
+//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: one thread
+//               per row (TMEM lane), online max/sum, P (bf16) written over
+//               the S columns; the O rescale is conditional (only when a
+//               row's maximum grows by more than 2^8) and done in TMEM.
+// The two tiles ping-pong, so one tile's softmax overlaps the other tile's
+// MMAs.  Each split writes a normalised partial (O / l, LSE) per row; the
+// per-beam stage and the LSE merge run in gr_beam_merge.cu.
+//
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// Every mbarrier wait is bounded: on expiry the CTA records a device error,
+// drains its in-flight copies and MMAs, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gr_common.cuh"
+#include "gr_ptx.cuh"
+
+namespace gr {
+
+namespace {
+
+constexpr int kBM = 128;           // rows per tile = TMEM lanes
+constexpr int kBN = 128;           // keys per block
+constexpr int kStages = 4;         // K/V ring slots
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// barrier slots
+constexpr int kBarKvFull = 0;               // [kStages]
+constexpr int kBarKvEmpty = kStages;        // [kStages]
+constexpr int kBarQFull = 2 * kStages;
+constexpr int kBarSFull = 2 * kStages + 1;  // [2]
+constexpr int kBarPFull = 2 * kStages + 3;  // [2]
+constexpr int kBarODone = 2 * kStages + 5;  // [2]
+constexpr int kBarFin = 2 * kStages + 7;
+constexpr int kNumBars = 2 * kStages + 8;
+
+template <int D>
+struct Cfg {
+    static constexpr int kHalves = D / 64;              // 64-element (128-byte) swizzle columns
+    static constexpr int kHalfBytes = kBM * 128;        // one 128-row x 64-element half
+    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kQOff = 0;                     // Q0, Q1
+    static constexpr int kKvOff = 2 * kTileBytes;       // ring
+    static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
+    static constexpr int kUsed = kBarOff + kNumBars * 8 + 16;
+    // >= 116 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits
+    static constexpr int kSmem = (kUsed + 1024 > 118 * 1024 ? kUsed + 1024 : 118 * 1024);
+    static constexpr int kOCol = 256;
+};
+
+struct TcParams {
+    CtxArgs a;
+    int bpt;    // beams per tile
+    int tiles;  // tiles per (request, kv head)
+};
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Warp-uniform bounded wait for an mbarrier phase: gives up after kSpinLimit
+// polls or one second, or as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    long long it = 0;
+    uint64_t t0 = 0;
+    while (true) {
+        const bool ok = ptx::mbar_try_wait(bar, parity);
+        if (__all_sync(kFullMask, ok)) return true;
+        ++it;
+        bool stop = (it > kSpinLimit) || (abort_flag != nullptr && *abort_flag != 0);
+        if ((it & 255) == 1) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > 1000000000ull) stop = true;
+        }
+        if (__any_sync(kFullMask, stop)) return false;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ctx_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ TcParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t bar0 = sbase + C::kBarOff;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kBarOff + kNumBars * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kBarOff + kNumBars * 8 + 4);
+
+    const Geometry &g = p.a.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = blockIdx.x;
+    const int kvh = blockIdx.y % g.Hkv, r = blockIdx.y / g.Hkv, sp = blockIdx.z;
+    const int tile0 = 2 * pair;
+    const bool t1_active = (tile0 + 1) < p.tiles;
+    const int rows_per_tile = p.bpt * g.G;
+
+    int len = p.a.ctx_len[r];
+    len = len < 0 ? 0 : (len > g.Lc_max ? g.Lc_max : len);
+    const int kbeg = sp * p.a.sp.split_len;
+    const int kend = min(kbeg + p.a.sp.split_len, len);
+    const int nb = kend > kbeg ? (kend - kbeg + kBN - 1) / kBN : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(bar(kBarKvFull + i), 1);
+            ptx::mbar_init(bar(kBarKvEmpty + i), 1);
+        }
+        ptx::mbar_init(bar(kBarQFull), 1);
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(kBarSFull + t), 1);
+            ptx::mbar_init(bar(kBarPFull + t), 128);
+            ptx::mbar_init(bar(kBarODone + t), 1);
+        }
+        ptx::mbar_init(bar(kBarFin), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (lane == 0) raise_device_error(p.a.err, kDevErrTimeout);
+    };
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        int issued = 0;
+        bool ok = true;
+        if (nb > 0) {
+            // rows of a tile past bpt*G are never loaded: keep them zero
+            if (rows_per_tile < kBM) {
+                const int tail = (kBM - rows_per_tile) * 128;
+                for (int t = 0; t < 2; ++t)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        for (int off = lane * 16; off < tail; off += 32 * 16)
+                            *reinterpret_cast<uint4 *>(smem + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes +
+                                                       rows_per_tile * 128 + off) = make_uint4(0, 0, 0, 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                ptx::prefetch_tmap(&tm_q);
+                ptx::prefetch_tmap(&tm_k);
+                ptx::prefetch_tmap(&tm_v);
+                const int nt = t1_active ? 2 : 1;
+                ptx::mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)(nt * C::kHalves * rows_per_tile * 128));
+                for (int t = 0; t < nt; ++t)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        ptx::tma_load_4d(sbase + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &tm_q,
+                                         bar(kBarQFull), h * 64, kvh * g.G, (tile0 + t) * p.bpt, r);
+            }
+            __syncwarp();
+            for (int n = 0; n < 2 * nb; ++n) {
+                const int s = n % kStages;
+                if (!wait_warp(bar(kBarKvEmpty + s), ((n / kStages) & 1) ^ 1, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar(kBarKvFull + s), (uint32_t)C::kTileBytes);
+                    const CUtensorMap *tm = (n & 1) ? &tm_v : &tm_k;
+                    const int key = kbeg + (n >> 1) * kBN;
+                    for (int h = 0; h < C::kHalves; ++h)
+                        ptx::tma_load_4d(sbase + C::kKvOff + s * C::kTileBytes + h * C::kHalfBytes, tm,
+                                         bar(kBarKvFull + s), h * 64, key, kvh, r);
+                }
+                __syncwarp();
+                issued = n + 1;
+            }
+            if (!ok) {
+                // drain: every copy in flight lands before the CTA leaves
+                wait_warp(bar(kBarQFull), 0, nullptr);
+                for (int n = issued - kStages < 0 ? 0 : issued - kStages; n < issued; ++n)
+                    wait_warp(bar(kBarKvFull + n % kStages), (n / kStages) & 1, nullptr);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (nb > 0) {
+            constexpr uint32_t kIdescQK = ptx::idesc_bf16(kBM, kBN, 0);
+            constexpr uint32_t kIdescPV = ptx::idesc_bf16(kBM, D, 1);
+            const int ntiles = t1_active ? 2 : 1;
+            auto kv_addr = [&](int s) -> uint32_t { return sbase + C::kKvOff + s * C::kTileBytes; };
+            auto issue_s = [&](int t, int s) {
+                if (lane == 0) {
+                    ptx::tc_fence_after();
+                    const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+                        ptx::mma_ss(tmem + t * kBN, ptx::smem_desc(qa + off, 16, 1024),
+                                    ptx::smem_desc(kv_addr(s) + off, 16, 1024), kIdescQK, kk > 0);
+                    }
+                    ptx::mma_commit(bar(kBarSFull + t));
+                }
+                __syncwarp();
+            };
+            auto issue_pv = [&](int t, int s, int i) {
+                if (lane == 0) {
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        ptx::mma_ts(tmem + C::kOCol + t * D, tmem + t * kBN + kk * 8,
+                                    ptx::smem_desc(kv_addr(s) + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
+                                    (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+            };
+
+            bool ok = wait_warp(bar(kBarQFull), 0, abort_flag) && wait_warp(bar(kBarKvFull + 0), 0, abort_flag);
+            if (ok) {
+                for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
+                if (lane == 0) ptx::mma_commit(bar(kBarKvEmpty + 0));
+                __syncwarp();
+            }
+            for (int i = 0; ok && i < nb; ++i) {
+                const int nv = 2 * i + 1, sv = nv % kStages;
+                if (!(ok = wait_warp(bar(kBarKvFull + sv), (nv / kStages) & 1, abort_flag))) break;
+                const int valid = min(kBN, kend - (kbeg + i * kBN));
+                if (valid < kBN) {
+                    // context positions past ctx_len hold anything: zero their V rows
+                    const int bytes = (kBN - valid) * 128;
+                    for (int h = 0; h < C::kHalves; ++h)
+                        for (int off = lane * 16; off < bytes; off += 32 * 16)
+                            *reinterpret_cast<uint4 *>(smem + C::kKvOff + sv * C::kTileBytes + h * C::kHalfBytes +
+                                                       valid * 128 + off) = make_uint4(0, 0, 0, 0);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                const bool has_next = (i + 1) < nb;
+                const int nk = 2 * (i + 1), sk = nk % kStages;
+                if (!(ok = wait_warp(bar(kBarPFull + 0), i & 1, abort_flag))) break;
+                issue_pv(0, sv, i);
+                if (i == nb - 1 && lane == 0) ptx::mma_commit(bar(kBarODone + 0));
+                if (has_next) {
+                    if (!(ok = wait_warp(bar(kBarKvFull + sk), (nk / kStages) & 1, abort_flag))) break;
+                    issue_s(0, sk);
+                }
+                if (t1_active) {
+                    if (!(ok = wait_warp(bar(kBarPFull + 1), i & 1, abort_flag))) break;
+                    issue_pv(1, sv, i);
+                    if (i == nb - 1 && lane == 0) ptx::mma_commit(bar(kBarODone + 1));
+                    if (has_next) issue_s(1, sk);
+                }
+                if (lane == 0) {
+                    ptx::mma_commit(bar(kBarKvEmpty + sv));
+                    if (has_next) ptx::mma_commit(bar(kBarKvEmpty + sk));
+                }
+                __syncwarp();
+            }
+            if (!ok) fail();
+            // no MMA may still be running when the TMEM is released
+            if (lane == 0) ptx::mma_commit(bar(kBarFin));
+            __syncwarp();
+            wait_warp(bar(kBarFin), 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + partial epilogue
+        const int t = warp >> 2, quarter = warp & 3;
+        const int m_local = quarter * 32 + lane;
+        const bool tile_active = (t == 0) || t1_active;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)(t * kBN);
+        const uint32_t tO = tmem + lane_off + (uint32_t)(C::kOCol + t * D);
+        const float c = g.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        if (tile_active && nb > 0) {
+            for (int i = 0; i < nb; ++i) {
+                if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
+                ptx::tc_fence_after();
+                uint32_t sv[kBN];
+#pragma unroll
+                for (int q4 = 0; q4 < kBN / 32; ++q4)
+                    ptx::tmem_ld32(tS + 32 * q4, &sv[32 * q4]);
+                ptx::tmem_wait_ld();
+                const int valid = min(kBN, kend - (kbeg + i * kBN));
+                if (valid < kBN) {
+#pragma unroll
+                    for (int j = 0; j < kBN; ++j)
+                        if (j >= valid) sv[j] = __float_as_uint(-INFINITY);
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kBN; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+                const float m_blk = mx * c;
+                if (i == 0) {
+                    m = m_blk;
+                } else {
+                    const bool need = m_blk > m + kRescaleThreshold;
+                    if (__any_sync(kFullMask, need)) {
+                        // O (and l) carry the old maximum: rescale them in TMEM
+                        const float f = need ? ptx::ex2(m - m_blk) : 1.f;
+#pragma unroll 1
+                        for (int q4 = 0; q4 < D / 16; ++q4) {
+                            uint32_t ov[16];
+                            ptx::tmem_ld16(tO + 16 * q4, ov);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                            ptx::tmem_st16(tO + 16 * q4, ov);
+                        }
+                        ptx::tmem_wait_st();
+                        l *= f;
+                        if (need) m = m_blk;
+                    }
+                }
+                const float neg_m = -m;
+                float sum = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[64 * half + 2 * j]), c, neg_m));
+                        const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[64 * half + 2 * j + 1]), c, neg_m));
+                        sum += p0 + p1;
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    // bf16 pairs over the first 64 S columns: P for the PV MMA
+                    ptx::tmem_st32(tS + 32 * half, pk);
+                }
+                l += sum;
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(kBarPFull + t));
+            }
+            if (ok) ok = wait_warp(bar(kBarODone + t), 0, abort_flag);
+            if (!ok) fail();
+            ptx::tc_fence_after();
+        }
+        if (tile_active) {
+            const int b = (tile0 + t) * p.bpt + m_local / g.G;
+            const bool row_ok = (m_local < rows_per_tile) && (b < g.W_s);
+            const long long n_rows = (long long)g.R * g.W_s * g.Hq;
+            const long long row = ((long long)r * g.W_s + b) * g.Hq + kvh * g.G + m_local % g.G;
+            float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
+            const bool have = ok && nb > 0;
+            const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+                uint32_t ov[32];
+                if (have) {
+                    ptx::tmem_ld32(tO + 32 * q4, ov);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] = 0u;
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(po + 32 * q4 + j) =
+                            make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
+                                        __uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+                }
+            }
+            if (row_ok)
+                p.a.part_lse[(long long)sp * n_rows + row] = (have && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool encode_4d(CUtensorMap *m, const void *base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+               const uint32_t box[4]) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint32_t elem[4] = {1, 1, 1, 1};
+    const CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides_bytes,
+                           box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
+    using C = Cfg<D>;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (dev < 64 && !attr_set[dev]) {
+            e = cudaFuncSetAttribute(ctx_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+    }
+    const Geometry &g = a.g;
+    CUtensorMap tq, tk, tv;
+    const uint64_t qd[4] = {(uint64_t)D, (uint64_t)g.Hq, (uint64_t)g.W_s, (uint64_t)g.R};
+    const uint64_t qs[3] = {(uint64_t)D * 2, (uint64_t)g.Hq * D * 2, (uint64_t)g.W_s * g.Hq * D * 2};
+    const uint32_t qb[4] = {64, (uint32_t)g.G, (uint32_t)bpt, 1};
+    const uint64_t kd[4] = {(uint64_t)D, (uint64_t)g.Lc_max, (uint64_t)g.Hkv, (uint64_t)g.R};
+    const uint64_t ks[3] = {(uint64_t)D * 2, (uint64_t)g.Lc_max * D * 2, (uint64_t)g.Hkv * g.Lc_max * D * 2};
+    const uint32_t kb[4] = {64, (uint32_t)kBN, 1, 1};
+    if (!encode_4d(&tq, a.q, qd, qs, qb) || !encode_4d(&tk, a.ctx_k, kd, ks, kb) ||
+        !encode_4d(&tv, a.ctx_v, kd, ks, kb))
+        return cudaErrorInvalidValue;
+    TcParams p;
+    p.a = a;
+    p.bpt = bpt;
+    p.tiles = tiles;
+    dim3 grid((tiles + 1) / 2, g.R * g.Hkv, a.sp.n_splits);
+    ctx_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_beams_per_tile(int G) { return kBM / G; }
+
+cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s) {
+    const int bpt = tc_beams_per_tile(a.g.G);
+    const int tiles = (a.g.W_s + bpt - 1) / bpt;
+    if (a.g.D == 128) return launch_d<128>(a, bpt, tiles, s);
+    return launch_d<64>(a, bpt, tiles, s);
+}
+
+}  // namespace gr

@@ -73,7 +73,7 @@ int make_geometry(const gr_attn_shape *s, const int32_t *widths, int32_t step, G
     if (s->num_q_heads % s->num_kv_heads != 0) return GR_ERR_BAD_SHAPE;
     if (s->head_dim != 64 && s->head_dim != 128) return GR_ERR_UNSUPPORTED;
     if (s->num_q_heads / s->num_kv_heads > 128) return GR_ERR_UNSUPPORTED;
-    if (!(std::isfinite(s->softmax_scale))) return GR_ERR_BAD_SHAPE;
+    if (!(std::isfinite(s->softmax_scale)) || !(s->softmax_scale > 0.f)) return GR_ERR_BAD_SHAPE;
     if (step < 0 || step >= s->step_capacity) return GR_ERR_BAD_SHAPE;
     if (step >= kMaxSteps) return GR_ERR_UNSUPPORTED;
     std::memset(g, 0, sizeof *g);
@@ -102,10 +102,12 @@ int make_geometry(const gr_attn_shape *s, const int32_t *widths, int32_t step, G
 
 enum class Path { kTensorCore, kSimt };
 
+// GR_ATTN_FORCE_PATH=simt selects the CUDA-core context stage (a cross-check
+// of the tensor-core kernel in tests); the tensor-core stage is the default.
 Path chosen_path() {
     const char *e = std::getenv("GR_ATTN_FORCE_PATH");
     if (e && std::strcmp(e, "simt") == 0) return Path::kSimt;
-    return Path::kSimt;
+    return Path::kTensorCore;
 }
 
 int forced_splits() {
@@ -134,7 +136,45 @@ SplitPlan plan_simt(const Geometry &g, int sm_count) {
     return p;
 }
 
-SplitPlan plan(const Geometry &g, int sm_count) { return plan_simt(g, sm_count); }
+// Split plan for the tensor-core context stage: one CTA per (request, kv head,
+// pair of 128-row tiles, split); splits are added until the grid covers the
+// SMs once (one CTA fits per SM).
+struct TcShape {
+    int bpt, tiles, pairs;
+};
+
+TcShape tc_shape(const Geometry &g) {
+    TcShape t;
+    t.bpt = tc_beams_per_tile(g.G);
+    t.tiles = (g.W_s + t.bpt - 1) / t.bpt;
+    t.pairs = (t.tiles + 1) / 2;
+    return t;
+}
+
+SplitPlan plan_tc(const Geometry &g, int sm_count) {
+    SplitPlan p{0, 0};
+    if (g.Lc_max == 0) return p;
+    constexpr int kKeyBlock = 128;
+    const int blocks = (g.Lc_max + kKeyBlock - 1) / kKeyBlock;
+    const long long ctas = (long long)tc_shape(g).pairs * g.R * g.Hkv;
+    int n = forced_splits();
+    if (n == 0) n = (int)std::max<long long>(1, (sm_count + ctas - 1) / ctas);
+    n = std::min(n, blocks);
+    const int per = (blocks + n - 1) / n;
+    p.split_len = per * kKeyBlock;
+    p.n_splits = (g.Lc_max + p.split_len - 1) / p.split_len;
+    return p;
+}
+
+SplitPlan plan(const Geometry &g, int sm_count) {
+    return chosen_path() == Path::kSimt ? plan_simt(g, sm_count) : plan_tc(g, sm_count);
+}
+
+long long context_ctas(const Geometry &g, const SplitPlan &sp) {
+    if (sp.n_splits == 0) return 0;
+    if (chosen_path() == Path::kSimt) return (long long)((g.W_s * g.G + 15) / 16) * g.R * g.Hkv * sp.n_splits;
+    return (long long)tc_shape(g).pairs * g.R * g.Hkv * sp.n_splits;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -237,7 +277,7 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         c.part_o = part_o;
         c.part_lse = part_lse;
         c.err = dev.err_ptr;
-        rc = cuda_status(launch_ctx_simt(c, s));
+        rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
         if (rc != GR_OK) return rc;
     }
     if ((rc = mark(1)) != GR_OK) return rc;
@@ -290,10 +330,10 @@ int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32
     rc = device_info(&dev);
     if (rc != GR_OK) return rc;
     const SplitPlan sp = plan(g, dev.sm_count);
-    info->path = 1;
+    info->path = chosen_path() == Path::kSimt ? 1 : 0;
     info->n_splits = sp.n_splits;
     info->split_len = sp.split_len;
-    info->context_ctas = sp.n_splits ? ((g.W_s * g.G + 15) / 16) * g.R * g.Hkv * sp.n_splits : 0;
+    info->context_ctas = (int32_t)context_ctas(g, sp);
     info->kernels = sp.n_splits ? 2 : 1;
     info->fused_merge = 0;
     return GR_OK;

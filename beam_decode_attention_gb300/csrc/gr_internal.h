@@ -67,4 +67,8 @@ cudaError_t launch_validate(const Geometry &g, const int32_t *beam_path, const i
 // gr_ctx_simt.cu  (CUDA-core context stage)
 cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
 
+// gr_ctx_tc.cu  (tensor-core context stage)
+int tc_beams_per_tile(int G);
+cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
+
 }  // namespace gr

@@ -35,7 +35,7 @@ import workloads  # noqa: E402
 METRIC = "µs/decode-step and TFLOP/s at BW=900, Lc=2048; % of bf16/HBM roofline"
 UNIT = "us/decode-step"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_simt.cu"]
+KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_tc.cu", "beam_decode_attention_gb300/csrc/gr_ptx.cuh"]
 
 
 def parse_args():

@@ -73,7 +73,7 @@ typedef struct {
     int32_t ctx_capacity;  /* Lc_max >= 0: context slots per (request, kv head) */
     int32_t step_capacity; /* S_max >= 1: decode-step slots in BeamKV/BeamPath */
     int32_t beam_capacity; /* W_max >= 1: beam slots per step */
-    float softmax_scale;   /* score scale (1/sqrt(D) for the Qwen3 heads) */
+    float softmax_scale;   /* score scale > 0 (1/sqrt(D) for the Qwen3 heads) */
 } gr_attn_shape;
 
 /*

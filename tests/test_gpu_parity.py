@@ -219,3 +219,23 @@ def test_error_statuses():
         gr.gr_decode_attn(dev.shape, dev.q[1], dev.ctx_k, dev.ctx_v, dev.ctx_len, dev.beam_k,
                           dev.beam_v, dev.beam_path, [2, 3], 1, out, lse, big)
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("path", ["simt", "default"])
+def test_context_stage_paths_agree_with_oracle(path):
+    """The CUDA-core context stage (GR_ATTN_FORCE_PATH=simt, the cross-check)
+    and the default tensor-core stage both meet the gate on a multi-tile
+    ragged case."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(2, 16, 8, 128, [520, 129], [9, 40, 140], seed=202)
+    if path == "simt":
+        os.environ["GR_ATTN_FORCE_PATH"] = "simt"
+    try:
+        dev = DeviceWorkload(inp)
+        assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)["path"] == (1 if path == "simt" else 0)
+        for step in range(3):
+            out, lse = dev.run(step, guard=16)
+            ref_out, ref_lse, _ = ORC.decode_attn(inp, step)
+            compare(out, lse, ref_out, ref_lse)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
