@@ -45,6 +45,8 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kFusedMaxTokens = 8;          // chain tokens the fused epilogue holds (steps < 8)
+constexpr int kPolyPairs = 3;               // of every 8 column pairs, exp2 by the FMA-pipe cubic
 
 // barrier slots
 constexpr int kBarKvFull = 0;               // [kStages]
@@ -64,7 +66,12 @@ struct Cfg {
     static constexpr int kQOff = 0;                     // Q0, Q1
     static constexpr int kKvOff = 2 * kTileBytes;       // ring
     static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
-    static constexpr int kUsed = kBarOff + kNumBars * 8 + 16;
+    // fused epilogue: per row and chain token, the token's score (base-2
+    // units) and BeamKV slot; per row a flag for a broken chain
+    static constexpr int kBeamX = kBarOff + kNumBars * 8 + 16;                  // float [kFusedMaxTokens][256]
+    static constexpr int kBeamSlot = kBeamX + kFusedMaxTokens * 2 * kBM * 4;    // int   [kFusedMaxTokens][256]
+    static constexpr int kBeamBad = kBeamSlot + kFusedMaxTokens * 2 * kBM * 4;  // int   [256]
+    static constexpr int kUsed = kBeamBad + 2 * kBM * 4;
     // >= 116 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits
     static constexpr int kSmem = (kUsed + 1024 > 118 * 1024 ? kUsed + 1024 : 118 * 1024);
     static constexpr int kOCol = 256;
@@ -91,14 +98,159 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
         const bool ok = ptx::mbar_try_wait(bar, parity);
         if (__all_sync(kFullMask, ok)) return true;
         ++it;
-        bool stop = (it > kSpinLimit) || (abort_flag != nullptr && *abort_flag != 0);
-        if ((it & 255) == 1) {
+        bool stop = (abort_flag != nullptr && *abort_flag != 0);
+        if ((it & 4095) == 0) {   // slow path: only long waits read the clock
             const uint64_t now = global_ns();
             if (t0 == 0) t0 = now;
             else if (now - t0 > 1000000000ull) stop = true;
+            if (it > kSpinLimit) stop = true;
         }
         if (__any_sync(kFullMask, stop)) return false;
     }
+}
+
+// Per-beam (unshared) stage for the row this thread owns, run before the
+// context loop while the first TMA loads are in flight: walk BeamPath back
+// from beam b (a_s = b, a_{t-1} = BeamPath[r, t, a_t]), score each chain
+// token against the query, and keep slot and score in shared memory for the
+// epilogue.  The parent index and the token's K row are fetched together,
+// so each token costs one memory round trip; the chain's V rows are
+// prefetched into L2 for the epilogue.
+template <int D>
+__device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, long long row, int b,
+                                              float *s_x, int *s_slot, int *s_bad, int ridx, bool q_in_smem,
+                                              uint32_t q_row_smem, int swz) {
+    const Geometry &g = a.g;
+    const uint4 *qg = reinterpret_cast<const uint4 *>(a.q + row * D);
+    // query chunk ch of this row: from the swizzled Q tile when it was loaded, else from global memory
+    auto q_chunk = [&](int ch) -> uint4 {
+        uint4 v;
+        if (q_in_smem) {
+            const uint32_t addr = q_row_smem + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ swz) * 16);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(addr));
+        } else {
+            v = __ldg(qg + ch);
+        }
+        return v;
+    };
+    int slot = b;
+    int bad = 0;
+    for (int t = g.step; t >= 0; --t) {
+        int par = 0;
+        if (t > 0) par = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot);
+        const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot) * g.Hkv + kvh) * D;
+        const uint4 *kr = reinterpret_cast<const uint4 *>(a.beam_k + kv_off);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off));
+        if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off + 64));
+        uint4 kv[D / 8];
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch) kv[ch] = __ldg(kr + ch);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch) {
+            const uint4 qv = q_chunk(ch);
+            d0 = fmaf(__uint_as_float(qv.x << 16), __uint_as_float(kv[ch].x << 16), d0);
+            d1 = fmaf(__uint_as_float(qv.x & 0xffff0000u), __uint_as_float(kv[ch].x & 0xffff0000u), d1);
+            d2 = fmaf(__uint_as_float(qv.y << 16), __uint_as_float(kv[ch].y << 16), d2);
+            d3 = fmaf(__uint_as_float(qv.y & 0xffff0000u), __uint_as_float(kv[ch].y & 0xffff0000u), d3);
+            d0 = fmaf(__uint_as_float(qv.z << 16), __uint_as_float(kv[ch].z << 16), d0);
+            d1 = fmaf(__uint_as_float(qv.z & 0xffff0000u), __uint_as_float(kv[ch].z & 0xffff0000u), d1);
+            d2 = fmaf(__uint_as_float(qv.w << 16), __uint_as_float(kv[ch].w << 16), d2);
+            d3 = fmaf(__uint_as_float(qv.w & 0xffff0000u), __uint_as_float(kv[ch].w & 0xffff0000u), d3);
+        }
+        s_x[t * 2 * kBM + ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
+        s_slot[t * 2 * kBM + ridx] = slot;
+        if (t > 0) {
+            if (par < 0 || par >= g.widths[t - 1]) {
+                bad = 1;   // a parent out of range: nothing past it is read
+                break;
+            }
+            slot = par;
+        }
+    }
+    s_bad[ridx] = bad;
+}
+
+// Merge for the row this thread owns (fused epilogue, single key split): the
+// context partial (O in TMEM, running max m in base-2 units, sum l) and the
+// chain tokens scored by beam_prologue are combined by log-sum-exp (the
+// merging stage), and the final bf16 row and fp32 LSE are written.
+// tcgen05.ld is warp-collective, so every lane takes part in the O loads.
+template <int D>
+__device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, long long row, bool row_ok,
+                                              bool have_ctx, float m_ctx, float l_ctx, uint32_t tO,
+                                              const float *s_x, const int *s_slot, const int *s_bad,
+                                              int ridx) {
+    const Geometry &g = a.g;
+    uint16_t *orow = a.out + row * D;
+    const bool bad = row_ok && s_bad[ridx] != 0;
+    if (!have_ctx) {
+        m_ctx = -INFINITY;
+        l_ctx = 0.f;
+    }
+    float m_tot = m_ctx;
+    if (row_ok && !bad)
+        for (int t = 0; t <= g.step; ++t) m_tot = fmaxf(m_tot, s_x[t * 2 * kBM + ridx]);
+    const float w_ctx = ptx::ex2(m_ctx - m_tot);   // no context: exp2(-inf) = 0
+    float L = l_ctx * w_ctx;
+    if (row_ok && !bad)
+        for (int t = 0; t <= g.step; ++t) L += ptx::ex2(s_x[t * 2 * kBM + ridx] - m_tot);
+    const float inv = row_ok && !bad ? 1.f / L : 0.f;
+#pragma unroll 1
+    for (int hh = 0; hh < D / 64; ++hh) {
+        float acc[64];
+        if (have_ctx) {
+            ptx::tmem_ld32(tO + 64 * hh, reinterpret_cast<uint32_t *>(&acc[0]));
+            ptx::tmem_ld32(tO + 64 * hh + 32, reinterpret_cast<uint32_t *>(&acc[32]));
+            ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int d = 0; d < 64; ++d) acc[d] = 0.f;
+        }
+        if (!row_ok || bad) continue;
+#pragma unroll
+        for (int d = 0; d < 64; ++d) acc[d] *= w_ctx;
+        for (int t = 0; t <= g.step; ++t) {
+            const float pw = ptx::ex2(s_x[t * 2 * kBM + ridx] - m_tot);
+            const long long kv_off =
+                ((((long long)r * g.S_max + t) * g.W_max + s_slot[t * 2 * kBM + ridx]) * g.Hkv + kvh) * D;
+            const uint4 *vr = reinterpret_cast<const uint4 *>(a.beam_v + kv_off + 64 * hh);
+            uint4 vv[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) vv[ch] = __ldg(vr + ch);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                acc[8 * ch + 0] = fmaf(pw, __uint_as_float(vv[ch].x << 16), acc[8 * ch + 0]);
+                acc[8 * ch + 1] = fmaf(pw, __uint_as_float(vv[ch].x & 0xffff0000u), acc[8 * ch + 1]);
+                acc[8 * ch + 2] = fmaf(pw, __uint_as_float(vv[ch].y << 16), acc[8 * ch + 2]);
+                acc[8 * ch + 3] = fmaf(pw, __uint_as_float(vv[ch].y & 0xffff0000u), acc[8 * ch + 3]);
+                acc[8 * ch + 4] = fmaf(pw, __uint_as_float(vv[ch].z << 16), acc[8 * ch + 4]);
+                acc[8 * ch + 5] = fmaf(pw, __uint_as_float(vv[ch].z & 0xffff0000u), acc[8 * ch + 5]);
+                acc[8 * ch + 6] = fmaf(pw, __uint_as_float(vv[ch].w << 16), acc[8 * ch + 6]);
+                acc[8 * ch + 7] = fmaf(pw, __uint_as_float(vv[ch].w & 0xffff0000u), acc[8 * ch + 7]);
+            }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + 64 * hh);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+            dst[ch] = make_uint4(pack_bf16x2(acc[8 * ch + 0] * inv, acc[8 * ch + 1] * inv),
+                                 pack_bf16x2(acc[8 * ch + 2] * inv, acc[8 * ch + 3] * inv),
+                                 pack_bf16x2(acc[8 * ch + 4] * inv, acc[8 * ch + 5] * inv),
+                                 pack_bf16x2(acc[8 * ch + 6] * inv, acc[8 * ch + 7] * inv));
+    }
+    if (!row_ok) return;
+    if (bad) {
+        // NaN marks a row whose chain is broken
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch)
+            reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+        a.lse[row] = __int_as_float(0x7fc00000);
+        raise_device_error(a.err, kDevErrBadParent);
+        return;
+    }
+    a.lse[row] = (m_tot + log2f(L)) * kLn2;
 }
 
 template <int D>
@@ -216,17 +368,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescQK = ptx::idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16(kBM, D, 1);
             const int ntiles = t1_active ? 2 : 1;
-            auto kv_addr = [&](int s) -> uint32_t { return sbase + C::kKvOff + s * C::kTileBytes; };
+            // Every descriptor is formed once: the issuing thread shares its SM
+            // sub-partition with two softmax warps, so each MMA must cost only
+            // an add and the instruction itself.  A k-step of 16 elements moves
+            // a K-major 128B-swizzled operand by 32 bytes inside the swizzle
+            // atom (and by a whole 64-column half after 4 steps), and the
+            // N-major V operand by 16 rows = 2048 bytes; in descriptor units
+            // (16 bytes) these are small constants added to the address field.
+            // Q tiles and ring slots are equally spaced, so a slot's descriptor
+            // is the first one's plus a multiple of the slot size.
+            const uint64_t dq0 = ptx::smem_desc(sbase + C::kQOff, 16, 1024);
+            const uint64_t dk0 = ptx::smem_desc(sbase + C::kKvOff, 16, 1024);
+            const uint64_t dv0 = ptx::smem_desc(sbase + C::kKvOff, C::kHalfBytes, 1024);
+            constexpr uint64_t kSlot = C::kTileBytes >> 4;
+            auto qk_step = [](int kk) -> uint64_t { return (uint64_t)((kk >> 2) * (C::kHalfBytes >> 4) + (kk & 3) * 2); };
             auto issue_s = [&](int t, int s) {
                 if (lane == 0) {
                     ptx::tc_fence_after();
-                    const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
+                    const uint64_t a0 = dq0 + (uint64_t)t * kSlot, b0 = dk0 + (uint64_t)s * kSlot;
+                    const uint32_t d = tmem + t * kBN;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-                        ptx::mma_ss(tmem + t * kBN, ptx::smem_desc(qa + off, 16, 1024),
-                                    ptx::smem_desc(kv_addr(s) + off, 16, 1024), kIdescQK, kk > 0);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        ptx::mma_ss(d, a0 + qk_step(kk), b0 + qk_step(kk), kIdescQK, kk > 0);
                     ptx::mma_commit(bar(kBarSFull + t));
                 }
                 __syncwarp();
@@ -234,11 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int t, int s, int i) {
                 if (lane == 0) {
                     ptx::tc_fence_after();
+                    const uint64_t b0 = dv0 + (uint64_t)s * kSlot;
+                    const uint32_t d = tmem + C::kOCol + t * D, a = tmem + t * kBN;
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        ptx::mma_ts(tmem + C::kOCol + t * D, tmem + t * kBN + kk * 8,
-                                    ptx::smem_desc(kv_addr(s) + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
-                                    (i > 0 || kk > 0) ? 1u : 0u);
+                        ptx::mma_ts(d, a + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, kk > 0 ? 1u : acc0);
                 }
                 __syncwarp();
             };
@@ -301,6 +465,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = g.scale_log2;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        float *s_x = reinterpret_cast<float *>(smem + C::kBeamX);
+        int *s_slot = reinterpret_cast<int *>(smem + C::kBeamSlot);
+        int *s_bad = reinterpret_cast<int *>(smem + C::kBeamBad);
+        const int ridx = t * kBM + m_local;
+        // this thread's row: beam b, query head kvh*G + m_local%G
+        auto row_beam = [&]() { return (tile0 + t) * p.bpt + m_local / g.G; };
+        auto row_valid = [&]() { return (m_local < rows_per_tile) && (row_beam() < g.W_s); };
+        auto row_index = [&]() {
+            return ((long long)r * g.W_s + row_beam()) * g.Hq + kvh * g.G + m_local % g.G;
+        };
+        if (tile_active && p.a.fused) {
+            // the Q tile lands first; the chain's scores use it from shared memory
+            if (nb > 0 && !wait_warp(bar(kBarQFull), 0, abort_flag)) fail();
+            if (row_valid())
+                beam_prologue<D>(p.a, r, kvh, row_index(), row_beam(), s_x, s_slot, s_bad, ridx, nb > 0,
+                                 sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u, m_local & 7);
+        }
         if (tile_active && nb > 0) {
             for (int i = 0; i < nb; ++i) {
                 if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
@@ -316,9 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kBN; ++j)
                         if (j >= valid) sv[j] = __float_as_uint(-INFINITY);
                 }
-                float mx = -INFINITY;
+                // row max: 8 chains of 3-input max over 16 columns each
+                float mx8[8];
 #pragma unroll
-                for (int j = 0; j < kBN; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+                for (int u = 0; u < 8; ++u) {
+                    float mu = fmaxf(__uint_as_float(sv[u]), __uint_as_float(sv[u + 8]));
+#pragma unroll
+                    for (int k = 2; k < 16; k += 2)
+                        mu = ptx::fmax3(mu, __uint_as_float(sv[u + 8 * k]), __uint_as_float(sv[u + 8 * k + 8]));
+                    mx8[u] = mu;
+                }
+                const float mx = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                                       fmaxf(ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_blk = mx * c;
                 if (i == 0) {
                     m = m_blk;
@@ -341,22 +531,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (need) m = m_blk;
                     }
                 }
+                // p = 2^(s*c - m): packed scale-and-subtract, then exp2 on the MUFU
+                // unit for most pairs and on the FMA pipe (cubic) for kPolyPairs of
+                // every 8, to balance the two pipes; packed row sums; bf16 pairs
+                // stored over the first 64 S columns as P for the PV MMA
                 const float neg_m = -m;
-                float sum = 0.f;
+                float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
+                for (int qtr = 0; qtr < 4; ++qtr) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float p0 = ptx::ex2(fmaf(__uint_as_float(sv[64 * half + 2 * j]), c, neg_m));
-                        const float p1 = ptx::ex2(fmaf(__uint_as_float(sv[64 * half + 2 * j + 1]), c, neg_m));
-                        sum += p0 + p1;
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 32 * qtr + 2 * j;
+                        float x0, x1, p0, p1;
+                        ptx::ffma2(x0, x1, __uint_as_float(sv[col]), __uint_as_float(sv[col + 1]), c, c, neg_m,
+                                   neg_m);
+                        if ((j & 7) < kPolyPairs) {
+                            ptx::ex2_poly2(x0, x1, p0, p1);
+                        } else {
+                            p0 = ptx::ex2(x0);
+                            p1 = ptx::ex2(x1);
+                        }
+                        ptx::fadd2(sa[j & 1], sb[j & 1], sa[j & 1], sb[j & 1], p0, p1);
                         pk[j] = pack_bf16x2(p0, p1);
                     }
-                    // bf16 pairs over the first 64 S columns: P for the PV MMA
-                    ptx::tmem_st32(tS + 32 * half, pk);
+                    ptx::tmem_st16(tS + 16 * qtr, pk);
                 }
-                l += sum;
+                l += (sa[0] + sa[1]) + (sb[0] + sb[1]);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(kBarPFull + t));
@@ -365,11 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) fail();
             ptx::tc_fence_after();
         }
-        if (tile_active) {
-            const int b = (tile0 + t) * p.bpt + m_local / g.G;
-            const bool row_ok = (m_local < rows_per_tile) && (b < g.W_s);
+        const bool row_ok = row_valid();
+        const long long row = row_index();
+        if (tile_active && p.a.fused) {
+            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx);
+        } else if (tile_active) {
             const long long n_rows = (long long)g.R * g.W_s * g.Hq;
-            const long long row = ((long long)r * g.W_s + b) * g.Hq + kvh * g.G + m_local % g.G;
             float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
             const bool have = ok && nb > 0;
             const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
@@ -472,6 +674,7 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
 }  // namespace
 
 int tc_beams_per_tile(int G) { return kBM / G; }
+int tc_fused_max_steps() { return kFusedMaxTokens; }
 
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s) {
     const int bpt = tc_beams_per_tile(a.g.G);

@@ -182,8 +182,16 @@ struct Layout {
     size_t part_o, part_lse, total;
 };
 
+// With a single key split (and a chain short enough for the kernel's
+// shared-memory scratch), the tensor-core kernel runs the per-beam stage and
+// the merge itself: no partials, no workspace, one kernel.
+bool fused_merge(const Geometry &g, const SplitPlan &p) {
+    return chosen_path() == Path::kTensorCore && p.n_splits == 1 && g.step < tc_fused_max_steps();
+}
+
 Layout workspace_layout(const Geometry &g, const SplitPlan &p) {
     Layout l{0, 0, 0};
+    if (fused_merge(g, p)) return l;
     const size_t rows = (size_t)g.R * g.W_s * g.Hq;
     const size_t o_bytes = (size_t)p.n_splits * rows * g.D * sizeof(float);
     const size_t lse_bytes = (size_t)p.n_splits * rows * sizeof(float);
@@ -277,10 +285,17 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         c.part_o = part_o;
         c.part_lse = part_lse;
         c.err = dev.err_ptr;
+        c.fused = fused_merge(g, sp) ? 1 : 0;
+        c.beam_k = static_cast<const uint16_t *>(beam_k);
+        c.beam_v = static_cast<const uint16_t *>(beam_v);
+        c.beam_path = beam_path;
+        c.out = static_cast<uint16_t *>(out);
+        c.lse = lse;
         rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
         if (rc != GR_OK) return rc;
     }
     if ((rc = mark(1)) != GR_OK) return rc;
+    if (fused_merge(g, sp)) return mark(2);
     MergeArgs m;
     m.g = g;
     m.n_splits = sp.n_splits;
@@ -334,8 +349,8 @@ int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32
     info->n_splits = sp.n_splits;
     info->split_len = sp.split_len;
     info->context_ctas = (int32_t)context_ctas(g, sp);
-    info->kernels = sp.n_splits ? 2 : 1;
-    info->fused_merge = 0;
+    info->fused_merge = fused_merge(g, sp) ? 1 : 0;
+    info->kernels = (sp.n_splits && !info->fused_merge) ? 2 : 1;
     return GR_OK;
 }
 

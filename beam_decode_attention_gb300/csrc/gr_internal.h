@@ -44,6 +44,13 @@ struct CtxArgs {
     float *part_o;    // fp32 [n_splits, R, W_s, Hq, D]  partial output, normalised
     float *part_lse;  // fp32 [n_splits, R, W_s, Hq]     partial LSE (natural log)
     int *err;
+    // fused epilogue (one key split): the kernel also runs the per-beam
+    // stage and the merge, and writes the final rows
+    int fused;
+    const uint16_t *beam_k, *beam_v;
+    const int32_t *beam_path;
+    uint16_t *out;
+    float *lse;
 };
 
 struct MergeArgs {
@@ -69,6 +76,7 @@ cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
 
 // gr_ctx_tc.cu  (tensor-core context stage)
 int tc_beams_per_tile(int G);
+int tc_fused_max_steps();  // the fused epilogue holds chains of steps < this
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 
 }  // namespace gr

@@ -156,13 +156,14 @@ def test_repeatable_and_stream():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_bad_parent_is_reported_not_followed():
+@pytest.mark.parametrize("splits", [1, 2])
+def test_bad_parent_is_reported_not_followed(splits):
     """A parent outside [0, W_{t-1}) is counted by gr_validate_beam_path; the
     decode call reads nothing out of range, writes NaN to the rows whose
     chain meets it, flags the device error word, and leaves the other rows
-    right."""
+    right -- in the fused single-split epilogue and in the split path."""
     import beam_decode_attention_gb300 as gr
-    inp = workloads.make_custom(2, 4, 2, 64, [10, 20], [3, 4, 5], seed=83)
+    inp = workloads.make_custom(2, 4, 2, 64, [150, 300], [3, 4, 5], seed=83)
     inp["beam_path"][1, 2, 2] = 4            # widths[1] == 4: out of range
     inp["beam_path"][0, 1, 0] = -3
     dev = DeviceWorkload(inp)
@@ -171,7 +172,12 @@ def test_bad_parent_is_reported_not_followed():
     gr.gr_validate_beam_path(dev.shape, dev.beam_path, dev.widths, 2, dev.ctx_len, bad)
     torch.cuda.synchronize()
     assert int(bad.item()) == 2
-    out, lse = dev.run(2)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    try:
+        assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)["fused_merge"] == (1 if splits == 1 else 0)
+        out, lse = dev.run(2)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
     assert gr.gr_get_device_error() == -8    # GR_ERR_BAD_BEAM_PATH
     assert gr.gr_get_device_error() == 0     # reading clears the word
 
@@ -200,11 +206,19 @@ def test_bad_parent_is_reported_not_followed():
 
 def test_error_statuses():
     import beam_decode_attention_gb300 as gr
-    inp = workloads.make_custom(1, 4, 2, 64, [10], [2, 2], seed=3)
+    inp = workloads.make_custom(1, 4, 2, 64, [300], [2, 2], seed=3)
     dev = DeviceWorkload(inp)
     out, lse = dev.outputs(1)
-    need = gr.gr_decode_attn_workspace_size(dev.shape, dev.widths, 1)
-    assert need > 0
+    os.environ["GR_ATTN_FORCE_SPLITS"] = "2"     # a plan that needs a workspace
+    try:
+        need = gr.gr_decode_attn_workspace_size(dev.shape, dev.widths, 1)
+        assert need > 0
+        _error_statuses(gr, dev, out, lse, need)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+
+
+def _error_statuses(gr, dev, out, lse, need):
     small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(gr.GRError) as e:
         gr.gr_decode_attn(dev.shape, dev.q[1], dev.ctx_k, dev.ctx_v, dev.ctx_len, dev.beam_k,
@@ -239,3 +253,18 @@ def test_context_stage_paths_agree_with_oracle(path):
             compare(out, lse, ref_out, ref_lse)
     finally:
         os.environ.pop("GR_ATTN_FORCE_PATH", None)
+
+
+def test_long_chain_beyond_fused_epilogue():
+    """Nine decode steps: longer than the fused epilogue holds, so the call
+    takes the partial + merge path; still exact against the oracle."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(2, 16, 8, 128, [200, 90], [2, 3, 4, 5, 6, 7, 8, 9, 10], seed=91)
+    dev = DeviceWorkload(inp)
+    assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 8)["fused_merge"] == 0
+    assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 7)["fused_merge"] in (0, 1)
+    for step in (7, 8):
+        out, lse = dev.run(step, guard=16)
+        ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+        compare(out, lse, ref_out, ref_lse)
+        assert np.array_equal(dev.ancestors(step), ref_anc)
