@@ -56,7 +56,8 @@ constexpr int kBarSFull = 2 * kStages + 1;  // [2]
 constexpr int kBarPFull = 2 * kStages + 3;  // [2]
 constexpr int kBarODone = 2 * kStages + 5;  // [2]
 constexpr int kBarFin = 2 * kStages + 7;
-constexpr int kNumBars = 2 * kStages + 8;
+constexpr int kBarVTail = 2 * kStages + 8;     // the tail block's V rows past ctx_len are zeroed
+constexpr int kNumBars = 2 * kStages + 9;
 
 template <int D>
 struct Cfg {
@@ -107,6 +108,22 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
         }
         if (__any_sync(kFullMask, stop)) return false;
     }
+}
+
+// Bounded wait by a single thread (the MMA issuer): same limits as wait_warp.
+__device__ __forceinline__ bool wait_lane(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    long long it = 0;
+    uint64_t t0 = 0;
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        ++it;
+        if (abort_flag != nullptr && *abort_flag != 0) return false;
+        if ((it & 4095) == 0) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > 1000000000ull || it > kSpinLimit) return false;
+        }
+    }
+    return true;
 }
 
 // Per-beam (unshared) stage for the row this thread owns, run before the
@@ -288,10 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarQFull), 1);
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(kBarSFull + t), 1);
-            ptx::mbar_init(bar(kBarPFull + t), 128);
+            ptx::mbar_init(bar(kBarPFull + t), 4);   // one arrival per softmax warp
             ptx::mbar_init(bar(kBarODone + t), 1);
         }
         ptx::mbar_init(bar(kBarFin), 1);
+        ptx::mbar_init(bar(kBarVTail), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -354,6 +372,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 issued = n + 1;
+                const int valid = min(kBN, kend - (kbeg + (n >> 1) * kBN));
+                if ((n & 1) && valid < kBN) {
+                    // the last block of the range: context positions past ctx_len hold
+                    // anything, so once the V block lands its rows past the end are
+                    // zeroed (P is 0 there, but 0 * NaN would not be)
+                    if (!wait_warp(bar(kBarKvFull + s), (n / kStages) & 1, abort_flag)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    const int bytes = (kBN - valid) * 128;
+                    for (int h = 0; h < C::kHalves; ++h)
+                        for (int off = lane * 16; off < bytes; off += 32 * 16)
+                            *reinterpret_cast<uint4 *>(smem + C::kKvOff + s * C::kTileBytes + h * C::kHalfBytes +
+                                                       valid * 128 + off) = make_uint4(0, 0, 0, 0);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(kBarVTail));
+                }
             }
             if (!ok) {
                 // drain: every copy in flight lands before the CTA leaves
@@ -364,95 +401,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (nb > 0) {
+        // One lane issues; lanes 1-31 go straight to the final barrier, so the
+        // issuing thread never reconverges its warp between MMA groups.
+        if (nb > 0 && lane == 0) {
             constexpr uint32_t kIdescQK = ptx::idesc_bf16(kBM, kBN, 0);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16(kBM, D, 1);
             const int ntiles = t1_active ? 2 : 1;
-            // Every descriptor is formed once: the issuing thread shares its SM
-            // sub-partition with two softmax warps, so each MMA must cost only
-            // an add and the instruction itself.  A k-step of 16 elements moves
-            // a K-major 128B-swizzled operand by 32 bytes inside the swizzle
-            // atom (and by a whole 64-column half after 4 steps), and the
-            // N-major V operand by 16 rows = 2048 bytes; in descriptor units
-            // (16 bytes) these are small constants added to the address field.
-            // Q tiles and ring slots are equally spaced, so a slot's descriptor
-            // is the first one's plus a multiple of the slot size.
+            // Every descriptor is formed once, so each MMA costs only an add and
+            // the instruction itself.  A k-step of 16 elements moves a K-major
+            // 128B-swizzled operand by 32 bytes inside the swizzle atom (and by a
+            // whole 64-column half after 4 steps), and the N-major V operand by 16
+            // rows = 2048 bytes; in descriptor units (16 bytes) these are small
+            // constants added to the address field.  Q tiles and ring slots are
+            // equally spaced, so a slot's descriptor is the first one's plus a
+            // multiple of the slot size.
             const uint64_t dq0 = ptx::smem_desc(sbase + C::kQOff, 16, 1024);
             const uint64_t dk0 = ptx::smem_desc(sbase + C::kKvOff, 16, 1024);
             const uint64_t dv0 = ptx::smem_desc(sbase + C::kKvOff, C::kHalfBytes, 1024);
             constexpr uint64_t kSlot = C::kTileBytes >> 4;
             auto qk_step = [](int kk) -> uint64_t { return (uint64_t)((kk >> 2) * (C::kHalfBytes >> 4) + (kk & 3) * 2); };
             auto issue_s = [&](int t, int s) {
-                if (lane == 0) {
-                    ptx::tc_fence_after();
-                    const uint64_t a0 = dq0 + (uint64_t)t * kSlot, b0 = dk0 + (uint64_t)s * kSlot;
-                    const uint32_t d = tmem + t * kBN;
+                ptx::tc_fence_after();
+                const uint64_t a0 = dq0 + (uint64_t)t * kSlot, b0 = dk0 + (uint64_t)s * kSlot;
+                const uint32_t d = tmem + t * kBN;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        ptx::mma_ss(d, a0 + qk_step(kk), b0 + qk_step(kk), kIdescQK, kk > 0);
-                    ptx::mma_commit(bar(kBarSFull + t));
-                }
-                __syncwarp();
+                for (int kk = 0; kk < D / 16; ++kk) ptx::mma_ss(d, a0 + qk_step(kk), b0 + qk_step(kk), kIdescQK, kk > 0);
+                ptx::mma_commit(bar(kBarSFull + t));
             };
             auto issue_pv = [&](int t, int s, int i) {
-                if (lane == 0) {
-                    ptx::tc_fence_after();
-                    const uint64_t b0 = dv0 + (uint64_t)s * kSlot;
-                    const uint32_t d = tmem + C::kOCol + t * D, a = tmem + t * kBN;
-                    const uint32_t acc0 = i > 0 ? 1u : 0u;
+                ptx::tc_fence_after();
+                const uint64_t b0 = dv0 + (uint64_t)s * kSlot;
+                const uint32_t d = tmem + C::kOCol + t * D, a = tmem + t * kBN;
+                const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        ptx::mma_ts(d, a + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, kk > 0 ? 1u : acc0);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts(d, a + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, kk > 0 ? 1u : acc0);
             };
 
-            bool ok = wait_warp(bar(kBarQFull), 0, abort_flag) && wait_warp(bar(kBarKvFull + 0), 0, abort_flag);
+            bool ok = wait_lane(bar(kBarQFull), 0, abort_flag) && wait_lane(bar(kBarKvFull + 0), 0, abort_flag);
             if (ok) {
                 for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
-                if (lane == 0) ptx::mma_commit(bar(kBarKvEmpty + 0));
-                __syncwarp();
+                ptx::mma_commit(bar(kBarKvEmpty + 0));
             }
             for (int i = 0; ok && i < nb; ++i) {
                 const int nv = 2 * i + 1, sv = nv % kStages;
-                if (!(ok = wait_warp(bar(kBarKvFull + sv), (nv / kStages) & 1, abort_flag))) break;
                 const int valid = min(kBN, kend - (kbeg + i * kBN));
-                if (valid < kBN) {
-                    // context positions past ctx_len hold anything: zero their V rows
-                    const int bytes = (kBN - valid) * 128;
-                    for (int h = 0; h < C::kHalves; ++h)
-                        for (int off = lane * 16; off < bytes; off += 32 * 16)
-                            *reinterpret_cast<uint4 *>(smem + C::kKvOff + sv * C::kTileBytes + h * C::kHalfBytes +
-                                                       valid * 128 + off) = make_uint4(0, 0, 0, 0);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                }
+                // a tail block's V is usable once the producer has zeroed its rows past the end
+                if (!(ok = (valid < kBN) ? wait_lane(bar(kBarVTail), 0, abort_flag)
+                                         : wait_lane(bar(kBarKvFull + sv), (nv / kStages) & 1, abort_flag)))
+                    break;
                 const bool has_next = (i + 1) < nb;
                 const int nk = 2 * (i + 1), sk = nk % kStages;
-                if (!(ok = wait_warp(bar(kBarPFull + 0), i & 1, abort_flag))) break;
+                if (!(ok = wait_lane(bar(kBarPFull + 0), i & 1, abort_flag))) break;
                 issue_pv(0, sv, i);
-                if (i == nb - 1 && lane == 0) ptx::mma_commit(bar(kBarODone + 0));
+                if (i == nb - 1) ptx::mma_commit(bar(kBarODone + 0));
                 if (has_next) {
-                    if (!(ok = wait_warp(bar(kBarKvFull + sk), (nk / kStages) & 1, abort_flag))) break;
+                    if (!(ok = wait_lane(bar(kBarKvFull + sk), (nk / kStages) & 1, abort_flag))) break;
                     issue_s(0, sk);
                 }
                 if (t1_active) {
-                    if (!(ok = wait_warp(bar(kBarPFull + 1), i & 1, abort_flag))) break;
+                    if (!(ok = wait_lane(bar(kBarPFull + 1), i & 1, abort_flag))) break;
                     issue_pv(1, sv, i);
-                    if (i == nb - 1 && lane == 0) ptx::mma_commit(bar(kBarODone + 1));
+                    if (i == nb - 1) ptx::mma_commit(bar(kBarODone + 1));
                     if (has_next) issue_s(1, sk);
                 }
-                if (lane == 0) {
-                    ptx::mma_commit(bar(kBarKvEmpty + sv));
-                    if (has_next) ptx::mma_commit(bar(kBarKvEmpty + sk));
-                }
-                __syncwarp();
+                ptx::mma_commit(bar(kBarKvEmpty + sv));
+                if (has_next) ptx::mma_commit(bar(kBarKvEmpty + sk));
             }
-            if (!ok) fail();
+            if (!ok) {
+                *abort_flag = 1;
+                raise_device_error(p.a.err, kDevErrTimeout);
+            }
             // no MMA may still be running when the TMEM is released
-            if (lane == 0) ptx::mma_commit(bar(kBarFin));
-            __syncwarp();
-            wait_warp(bar(kBarFin), 0, nullptr);
+            ptx::mma_commit(bar(kBarFin));
+            wait_lane(bar(kBarFin), 0, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax + partial epilogue
@@ -558,9 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_st16(tS + 16 * qtr, pk);
                 }
                 l += (sa[0] + sa[1]) + (sb[0] + sb[1]);
+                // P is in TMEM: each thread's stores complete and are fenced, the
+                // warp synchronises, and one lane signals for the warp
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(kBarPFull + t));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarPFull + t));
             }
             if (ok) ok = wait_warp(bar(kBarODone + t), 0, abort_flag);
             if (!ok) fail();
