@@ -42,11 +42,14 @@ constexpr int kBN = 128;           // keys per block
 constexpr int kStages = 4;         // K/V ring slots
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kBeamWarp = 10;               // warps 10 and 11: per-beam stage
+constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kFusedMaxTokens = 8;          // chain tokens the fused epilogue holds (steps < 8)
-constexpr int kPolyPairs = 3;               // of every 8 column pairs, exp2 by the FMA-pipe cubic
+// of every 8 column pairs, how many take exp2 from the FMA-pipe cubic instead
+// of the MUFU unit; on GB300 (ex2 at 32 lanes/clock/SM) all-MUFU measured fastest
+constexpr int kPolyPairs = 0;
 
 // barrier slots
 constexpr int kBarKvFull = 0;               // [kStages]
@@ -57,7 +60,8 @@ constexpr int kBarPFull = 2 * kStages + 3;  // [2]
 constexpr int kBarODone = 2 * kStages + 5;  // [2]
 constexpr int kBarFin = 2 * kStages + 7;
 constexpr int kBarVTail = 2 * kStages + 8;     // the tail block's V rows past ctx_len are zeroed
-constexpr int kNumBars = 2 * kStages + 9;
+constexpr int kBarBeam = 2 * kStages + 9;      // chain slots and scores are in shared memory
+constexpr int kNumBars = 2 * kStages + 10;
 
 template <int D>
 struct Cfg {
@@ -126,83 +130,115 @@ __device__ __forceinline__ bool wait_lane(uint32_t bar, uint32_t parity, volatil
     return true;
 }
 
-// Per-beam (unshared) stage for the row this thread owns, run before the
-// context loop while the first TMA loads are in flight: walk BeamPath back
-// from beam b (a_s = b, a_{t-1} = BeamPath[r, t, a_t]), score each chain
-// token against the query, and keep slot and score in shared memory for the
-// epilogue.  The parent index and the token's K row are fetched together,
-// so each token costs one memory round trip; the chain's V rows are
-// prefetched into L2 for the epilogue.
-template <int D>
-__device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, long long row, int b,
-                                              float *s_x, int *s_slot, int *s_bad, int ridx, bool q_in_smem,
-                                              uint32_t q_row_smem, int swz) {
+// One query row of the per-beam stage: its chain is walked by beam_prologue.
+struct BeamRow {
+    bool valid;      // a row of this call (inside the tile and the step's width)
+    long long row;   // global row index (r, beam, query head)
+    int beam;        // a_s: the row's beam at the current step
+    int ridx;        // the row's slot in the shared-memory tables
+    uint32_t q_smem; // the row's query in the swizzled Q tile
+    int swz;         // 128-byte swizzle phase of that row
+};
+
+// Per-beam (unshared) stage for NR rows at a time, run by the beam warps
+// while the context loop runs: walk BeamPath back from each row's beam
+// (a_s = b, a_{t-1} = BeamPath[r, t, a_t]), score each chain token against
+// the query (base-2 units), and keep slot and score in shared memory for the
+// epilogue.  The NR rows advance together, and a token's parent index and K
+// row are fetched together, so a token costs one memory round trip for all
+// NR rows; the chain's V rows are prefetched into L2 for the epilogue.
+template <int D, int NR>
+__device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, const BeamRow (&br)[NR],
+                                              bool q_in_smem, float *s_x, int *s_slot, int *s_bad) {
     const Geometry &g = a.g;
-    const uint4 *qg = reinterpret_cast<const uint4 *>(a.q + row * D);
-    // query chunk ch of this row: from the swizzled Q tile when it was loaded, else from global memory
-    auto q_chunk = [&](int ch) -> uint4 {
+    int slot[NR], bad[NR];
+    bool on[NR];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+        slot[k] = br[k].beam;
+        bad[k] = 0;
+        on[k] = br[k].valid;
+    }
+    // query chunk ch of row k: from the swizzled Q tile when it was loaded, else from global memory
+    auto q_chunk = [&](int k, int ch) -> uint4 {
         uint4 v;
         if (q_in_smem) {
-            const uint32_t addr = q_row_smem + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ swz) * 16);
+            const uint32_t addr =
+                br[k].q_smem + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ br[k].swz) * 16);
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                          : "r"(addr));
         } else {
-            v = __ldg(qg + ch);
+            v = __ldg(reinterpret_cast<const uint4 *>(a.q + br[k].row * D) + ch);
         }
         return v;
     };
-    int slot = b;
-    int bad = 0;
     for (int t = g.step; t >= 0; --t) {
-        int par = 0;
-        if (t > 0) par = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot);
-        const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot) * g.Hkv + kvh) * D;
-        const uint4 *kr = reinterpret_cast<const uint4 *>(a.beam_k + kv_off);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off));
-        if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off + 64));
-        uint4 kv[D / 8];
+        int par[NR];
+        uint4 kv[NR][D / 8];
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) kv[ch] = __ldg(kr + ch);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        for (int k = 0; k < NR; ++k) {
+            par[k] = 0;
+            if (!on[k]) continue;
+            if (t > 0) par[k] = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot[k]);
+            const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot[k]) * g.Hkv + kvh) * D;
+            const uint4 *kr = reinterpret_cast<const uint4 *>(a.beam_k + kv_off);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off));
+            if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off + 64));
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) {
-            const uint4 qv = q_chunk(ch);
-            d0 = fmaf(__uint_as_float(qv.x << 16), __uint_as_float(kv[ch].x << 16), d0);
-            d1 = fmaf(__uint_as_float(qv.x & 0xffff0000u), __uint_as_float(kv[ch].x & 0xffff0000u), d1);
-            d2 = fmaf(__uint_as_float(qv.y << 16), __uint_as_float(kv[ch].y << 16), d2);
-            d3 = fmaf(__uint_as_float(qv.y & 0xffff0000u), __uint_as_float(kv[ch].y & 0xffff0000u), d3);
-            d0 = fmaf(__uint_as_float(qv.z << 16), __uint_as_float(kv[ch].z << 16), d0);
-            d1 = fmaf(__uint_as_float(qv.z & 0xffff0000u), __uint_as_float(kv[ch].z & 0xffff0000u), d1);
-            d2 = fmaf(__uint_as_float(qv.w << 16), __uint_as_float(kv[ch].w << 16), d2);
-            d3 = fmaf(__uint_as_float(qv.w & 0xffff0000u), __uint_as_float(kv[ch].w & 0xffff0000u), d3);
+            for (int ch = 0; ch < D / 8; ++ch) kv[k][ch] = __ldg(kr + ch);
         }
-        s_x[t * 2 * kBM + ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
-        s_slot[t * 2 * kBM + ridx] = slot;
-        if (t > 0) {
-            if (par < 0 || par >= g.widths[t - 1]) {
-                bad = 1;   // a parent out of range: nothing past it is read
-                break;
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            if (!on[k]) continue;
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < D / 8; ++ch) {
+                const uint4 qv = q_chunk(k, ch);
+                const uint4 kc = kv[k][ch];
+                d0 = fmaf(__uint_as_float(qv.x << 16), __uint_as_float(kc.x << 16), d0);
+                d1 = fmaf(__uint_as_float(qv.x & 0xffff0000u), __uint_as_float(kc.x & 0xffff0000u), d1);
+                d2 = fmaf(__uint_as_float(qv.y << 16), __uint_as_float(kc.y << 16), d2);
+                d3 = fmaf(__uint_as_float(qv.y & 0xffff0000u), __uint_as_float(kc.y & 0xffff0000u), d3);
+                d0 = fmaf(__uint_as_float(qv.z << 16), __uint_as_float(kc.z << 16), d0);
+                d1 = fmaf(__uint_as_float(qv.z & 0xffff0000u), __uint_as_float(kc.z & 0xffff0000u), d1);
+                d2 = fmaf(__uint_as_float(qv.w << 16), __uint_as_float(kc.w << 16), d2);
+                d3 = fmaf(__uint_as_float(qv.w & 0xffff0000u), __uint_as_float(kc.w & 0xffff0000u), d3);
             }
-            slot = par;
+            s_x[t * 2 * kBM + br[k].ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
+            s_slot[t * 2 * kBM + br[k].ridx] = slot[k];
+            if (t > 0) {
+                if (par[k] < 0 || par[k] >= g.widths[t - 1]) {
+                    bad[k] = 1;   // a parent out of range: nothing past it is read
+                    on[k] = false;
+                } else {
+                    slot[k] = par[k];
+                }
+            }
         }
     }
-    s_bad[ridx] = bad;
+#pragma unroll
+    for (int k = 0; k < NR; ++k)
+        if (br[k].valid) s_bad[br[k].ridx] = bad[k];
 }
 
 // Merge for the row this thread owns (fused epilogue, single key split): the
 // context partial (O in TMEM, running max m in base-2 units, sum l) and the
 // chain tokens scored by beam_prologue are combined by log-sum-exp (the
-// merging stage), and the final bf16 row and fp32 LSE are written.
-// tcgen05.ld is warp-collective, so every lane takes part in the O loads.
+// merging stage), and the final bf16 row and fp32 LSE are written.  The
+// chain's V rows were prefetched into L2 by the beam warps; they are loaded
+// two tokens at a time.  tcgen05.ld is warp-collective, so every lane takes
+// part in the O loads.  beam_ok is false when the beam warps gave up (the
+// call already reports a timeout): the row is then written as NaN without
+// reading the chain tables.
 template <int D>
 __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, long long row, bool row_ok,
                                               bool have_ctx, float m_ctx, float l_ctx, uint32_t tO,
-                                              const float *s_x, const int *s_slot, const int *s_bad,
-                                              int ridx) {
+                                              const float *s_x, const int *s_slot, const int *s_bad, int ridx,
+                                              bool beam_ok) {
     const Geometry &g = a.g;
     uint16_t *orow = a.out + row * D;
-    const bool bad = row_ok && s_bad[ridx] != 0;
+    const bool bad = row_ok && (!beam_ok || s_bad[ridx] != 0);
     if (!have_ctx) {
         m_ctx = -INFINITY;
         l_ctx = 0.f;
@@ -227,44 +263,58 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
             for (int d = 0; d < 64; ++d) acc[d] = 0.f;
         }
         if (!row_ok || bad) continue;
+        const float wc = w_ctx * inv;
 #pragma unroll
-        for (int d = 0; d < 64; ++d) acc[d] *= w_ctx;
-        for (int t = 0; t <= g.step; ++t) {
-            const float pw = ptx::ex2(s_x[t * 2 * kBM + ridx] - m_tot);
-            const long long kv_off =
-                ((((long long)r * g.S_max + t) * g.W_max + s_slot[t * 2 * kBM + ridx]) * g.Hkv + kvh) * D;
-            const uint4 *vr = reinterpret_cast<const uint4 *>(a.beam_v + kv_off + 64 * hh);
-            uint4 vv[8];
+        for (int d = 0; d < 64; ++d) acc[d] *= wc;
+        // chain tokens two at a time: both V row halves are in flight together
+        for (int t0 = 0; t0 <= g.step; t0 += 2) {
+            const bool two = t0 < g.step;
+            uint4 va[8], vb[8];
+            const float pa = ptx::ex2(s_x[t0 * 2 * kBM + ridx] - m_tot) * inv;
+            const float pb = two ? ptx::ex2(s_x[(t0 + 1) * 2 * kBM + ridx] - m_tot) * inv : 0.f;
+            const uint4 *ra = reinterpret_cast<const uint4 *>(
+                a.beam_v + ((((long long)r * g.S_max + t0) * g.W_max + s_slot[t0 * 2 * kBM + ridx]) * g.Hkv + kvh) * D +
+                64 * hh);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) vv[ch] = __ldg(vr + ch);
+            for (int c = 0; c < 8; ++c) va[c] = __ldg(ra + c);
+            if (two) {
+                const uint4 *rb = reinterpret_cast<const uint4 *>(
+                    a.beam_v +
+                    ((((long long)r * g.S_max + t0 + 1) * g.W_max + s_slot[(t0 + 1) * 2 * kBM + ridx]) * g.Hkv + kvh) *
+                        D +
+                    64 * hh);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                acc[8 * ch + 0] = fmaf(pw, __uint_as_float(vv[ch].x << 16), acc[8 * ch + 0]);
-                acc[8 * ch + 1] = fmaf(pw, __uint_as_float(vv[ch].x & 0xffff0000u), acc[8 * ch + 1]);
-                acc[8 * ch + 2] = fmaf(pw, __uint_as_float(vv[ch].y << 16), acc[8 * ch + 2]);
-                acc[8 * ch + 3] = fmaf(pw, __uint_as_float(vv[ch].y & 0xffff0000u), acc[8 * ch + 3]);
-                acc[8 * ch + 4] = fmaf(pw, __uint_as_float(vv[ch].z << 16), acc[8 * ch + 4]);
-                acc[8 * ch + 5] = fmaf(pw, __uint_as_float(vv[ch].z & 0xffff0000u), acc[8 * ch + 5]);
-                acc[8 * ch + 6] = fmaf(pw, __uint_as_float(vv[ch].w << 16), acc[8 * ch + 6]);
-                acc[8 * ch + 7] = fmaf(pw, __uint_as_float(vv[ch].w & 0xffff0000u), acc[8 * ch + 7]);
+                for (int c = 0; c < 8; ++c) vb[c] = __ldg(rb + c);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) vb[c] = make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t ua[4] = {va[c].x, va[c].y, va[c].z, va[c].w};
+                const uint32_t ub[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float &lo = acc[8 * c + 2 * e], &hi = acc[8 * c + 2 * e + 1];
+                    lo = fmaf(pb, __uint_as_float(ub[e] << 16), fmaf(pa, __uint_as_float(ua[e] << 16), lo));
+                    hi = fmaf(pb, __uint_as_float(ub[e] & 0xffff0000u), fmaf(pa, __uint_as_float(ua[e] & 0xffff0000u), hi));
+                }
             }
         }
         uint4 *dst = reinterpret_cast<uint4 *>(orow + 64 * hh);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            dst[ch] = make_uint4(pack_bf16x2(acc[8 * ch + 0] * inv, acc[8 * ch + 1] * inv),
-                                 pack_bf16x2(acc[8 * ch + 2] * inv, acc[8 * ch + 3] * inv),
-                                 pack_bf16x2(acc[8 * ch + 4] * inv, acc[8 * ch + 5] * inv),
-                                 pack_bf16x2(acc[8 * ch + 6] * inv, acc[8 * ch + 7] * inv));
+        for (int c = 0; c < 8; ++c)
+            dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                                pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
     }
     if (!row_ok) return;
     if (bad) {
         // NaN marks a row whose chain is broken
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch)
-            reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+        for (int c = 0; c < D / 8; ++c)
+            reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
         a.lse[row] = __int_as_float(0x7fc00000);
-        raise_device_error(a.err, kDevErrBadParent);
+        if (beam_ok) raise_device_error(a.err, kDevErrBadParent);
         return;
     }
     a.lse[row] = (m_tot + log2f(L)) * kLn2;
@@ -297,7 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kend = min(kbeg + p.a.sp.split_len, len);
     const int nb = kend > kbeg ? (kend - kbeg + kBN - 1) / kBN : 0;
 
-    if (threadIdx.x == 0) {
+    // The producer initialises the barriers and starts the loads that the first
+    // S needs (the Q tiles and K of block 0) while warp 9 allocates TMEM.
+    if (warp == kProducerWarp && lane == 0) {
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(bar(kBarKvFull + i), 1);
             ptx::mbar_init(bar(kBarKvEmpty + i), 1);
@@ -310,8 +362,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(bar(kBarFin), 1);
         ptx::mbar_init(bar(kBarVTail), 1);
+        ptx::mbar_init(bar(kBarBeam), 2);   // one arrival per beam warp
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == kProducerWarp && nb > 0) {
+        __syncwarp();
+        // rows of a tile past bpt*G are never loaded: keep them zero
+        if (rows_per_tile < kBM) {
+            const int tail = (kBM - rows_per_tile) * 128;
+            for (int t = 0; t < 2; ++t)
+                for (int h = 0; h < C::kHalves; ++h)
+                    for (int off = lane * 16; off < tail; off += 32 * 16)
+                        *reinterpret_cast<uint4 *>(smem + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes +
+                                                   rows_per_tile * 128 + off) = make_uint4(0, 0, 0, 0);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+        }
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_q);
+            ptx::prefetch_tmap(&tm_k);
+            ptx::prefetch_tmap(&tm_v);
+            const int nt = t1_active ? 2 : 1;
+            ptx::mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)(nt * C::kHalves * rows_per_tile * 128));
+            for (int t = 0; t < nt; ++t)
+                for (int h = 0; h < C::kHalves; ++h)
+                    ptx::tma_load_4d(sbase + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &tm_q, bar(kBarQFull),
+                                     h * 64, kvh * g.G, (tile0 + t) * p.bpt, r);
+            // load 0 (K of block 0) into ring slot 0, which starts out free
+            ptx::mbar_arrive_expect_tx(bar(kBarKvFull + 0), (uint32_t)C::kTileBytes);
+            for (int h = 0; h < C::kHalves; ++h)
+                ptx::tma_load_4d(sbase + C::kKvOff + h * C::kHalfBytes, &tm_k, bar(kBarKvFull + 0), h * 64, kbeg, kvh,
+                                 r);
+        }
+        __syncwarp();
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -329,33 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
-        int issued = 0;
+        int issued = 1;   // the Q tiles and load 0 went out before the CTA-wide barrier
         bool ok = true;
         if (nb > 0) {
-            // rows of a tile past bpt*G are never loaded: keep them zero
-            if (rows_per_tile < kBM) {
-                const int tail = (kBM - rows_per_tile) * 128;
-                for (int t = 0; t < 2; ++t)
-                    for (int h = 0; h < C::kHalves; ++h)
-                        for (int off = lane * 16; off < tail; off += 32 * 16)
-                            *reinterpret_cast<uint4 *>(smem + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes +
-                                                       rows_per_tile * 128 + off) = make_uint4(0, 0, 0, 0);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
-                ptx::prefetch_tmap(&tm_q);
-                ptx::prefetch_tmap(&tm_k);
-                ptx::prefetch_tmap(&tm_v);
-                const int nt = t1_active ? 2 : 1;
-                ptx::mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)(nt * C::kHalves * rows_per_tile * 128));
-                for (int t = 0; t < nt; ++t)
-                    for (int h = 0; h < C::kHalves; ++h)
-                        ptx::tma_load_4d(sbase + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &tm_q,
-                                         bar(kBarQFull), h * 64, kvh * g.G, (tile0 + t) * p.bpt, r);
-            }
-            __syncwarp();
-            for (int n = 0; n < 2 * nb; ++n) {
+            for (int n = 1; n < 2 * nb; ++n) {
                 const int s = n % kStages;
                 if (!wait_warp(bar(kBarKvEmpty + s), ((n / kStages) & 1) ^ 1, abort_flag)) {
                     fail();
@@ -443,29 +505,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
                 ptx::mma_commit(bar(kBarKvEmpty + 0));
             }
+            // A thread that has just issued MMAs stalls on its next mbarrier
+            // wait until they have drained into the tensor pipe, which then runs
+            // dry: every wait here costs pipe time.  So the issuer waits only for
+            // P; the softmax warps certify, before they signal P_t(i), that V(i)
+            // and K(i+1) have landed.
             for (int i = 0; ok && i < nb; ++i) {
-                const int nv = 2 * i + 1, sv = nv % kStages;
-                const int valid = min(kBN, kend - (kbeg + i * kBN));
-                // a tail block's V is usable once the producer has zeroed its rows past the end
-                if (!(ok = (valid < kBN) ? wait_lane(bar(kBarVTail), 0, abort_flag)
-                                         : wait_lane(bar(kBarKvFull + sv), (nv / kStages) & 1, abort_flag)))
-                    break;
+                const int sv = (2 * i + 1) % kStages;
                 const bool has_next = (i + 1) < nb;
-                const int nk = 2 * (i + 1), sk = nk % kStages;
+                const int sk = (2 * (i + 1)) % kStages;
                 if (!(ok = wait_lane(bar(kBarPFull + 0), i & 1, abort_flag))) break;
                 issue_pv(0, sv, i);
                 if (i == nb - 1) ptx::mma_commit(bar(kBarODone + 0));
-                if (has_next) {
-                    if (!(ok = wait_lane(bar(kBarKvFull + sk), (nk / kStages) & 1, abort_flag))) break;
-                    issue_s(0, sk);
-                }
+                if (has_next) issue_s(0, sk);
                 if (t1_active) {
                     if (!(ok = wait_lane(bar(kBarPFull + 1), i & 1, abort_flag))) break;
                     issue_pv(1, sv, i);
                     if (i == nb - 1) ptx::mma_commit(bar(kBarODone + 1));
-                    if (has_next) issue_s(1, sk);
                 }
+                // V(i)'s slot is free once the last PV that reads it is done
                 ptx::mma_commit(bar(kBarKvEmpty + sv));
+                if (t1_active && has_next) issue_s(1, sk);
                 if (has_next) ptx::mma_commit(bar(kBarKvEmpty + sk));
             }
             if (!ok) {
@@ -475,6 +535,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             // no MMA may still be running when the TMEM is released
             ptx::mma_commit(bar(kBarFin));
             wait_lane(bar(kBarFin), 0, nullptr);
+        }
+    } else if (warp >= kBeamWarp) {
+        // ------------------------------------------------------------ per-beam stage
+        // 64 threads, four rows each (rows b and b + 64 of each tile, two at a
+        // time), while the context loop runs; then one arrival per warp.
+        if (p.a.fused) {
+            bool okq = nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag);   // q is read from the Q tile
+            if (!okq) {
+                fail();
+            } else {
+                float *s_x = reinterpret_cast<float *>(smem + C::kBeamX);
+                int *s_slot = reinterpret_cast<int *>(smem + C::kBeamSlot);
+                int *s_bad = reinterpret_cast<int *>(smem + C::kBeamBad);
+                const int b = (warp - kBeamWarp) * 32 + lane;
+                for (int t = 0; t < 2; ++t) {
+                    if (t == 1 && !t1_active) break;
+                    BeamRow br[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int m_local = b + 64 * k;
+                        const int beam = (tile0 + t) * p.bpt + m_local / g.G;
+                        br[k].valid = (m_local < rows_per_tile) && (beam < g.W_s);
+                        br[k].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
+                        br[k].beam = beam;
+                        br[k].ridx = t * kBM + m_local;
+                        br[k].q_smem = sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u;
+                        br[k].swz = m_local & 7;
+                    }
+                    beam_prologue<D, 2>(p.a, r, kvh, br, nb > 0, s_x, s_slot, s_bad);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarBeam));
         }
     } else {
         // ------------------------------------------------------------ softmax + partial epilogue
@@ -491,21 +584,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         int *s_slot = reinterpret_cast<int *>(smem + C::kBeamSlot);
         int *s_bad = reinterpret_cast<int *>(smem + C::kBeamBad);
         const int ridx = t * kBM + m_local;
+
         // this thread's row: beam b, query head kvh*G + m_local%G
         auto row_beam = [&]() { return (tile0 + t) * p.bpt + m_local / g.G; };
         auto row_valid = [&]() { return (m_local < rows_per_tile) && (row_beam() < g.W_s); };
         auto row_index = [&]() {
             return ((long long)r * g.W_s + row_beam()) * g.Hq + kvh * g.G + m_local % g.G;
         };
-        if (tile_active && p.a.fused) {
-            // the Q tile lands first; the chain's scores use it from shared memory
-            if (nb > 0 && !wait_warp(bar(kBarQFull), 0, abort_flag)) fail();
-            if (row_valid())
-                beam_prologue<D>(p.a, r, kvh, row_index(), row_beam(), s_x, s_slot, s_bad, ridx, nb > 0,
-                                 sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u, m_local & 7);
-        }
         if (tile_active && nb > 0) {
             for (int i = 0; i < nb; ++i) {
+                // P_t(i) also tells the issuer that V(i) and K(i+1) have landed (the
+                // issuer itself waits only for P).  One lane per tile looks while the
+                // warp would wait for S anyway, and waits after the pass only if a
+                // load was still in flight.
+                const int valid = min(kBN, kend - (kbeg + i * kBN));
+                const int nv = 2 * i + 1, nk = 2 * (i + 1);
+                auto v_bar = [&]() { return valid < kBN ? bar(kBarVTail) : bar(kBarKvFull + nv % kStages); };
+                auto v_par = [&]() -> uint32_t { return valid < kBN ? 0u : (uint32_t)((nv / kStages) & 1); };
+                bool kv_seen = true;
+                if (quarter == 0 && lane == 0)
+                    kv_seen = ptx::mbar_test_wait(v_bar(), v_par()) &&
+                              (i + 1 >= nb || ptx::mbar_test_wait(bar(kBarKvFull + nk % kStages), (nk / kStages) & 1));
                 if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
                 ptx::tc_fence_after();
                 uint32_t sv[kBN];
@@ -513,77 +612,90 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q4 = 0; q4 < kBN / 32; ++q4)
                     ptx::tmem_ld32(tS + 32 * q4, &sv[32 * q4]);
                 ptx::tmem_wait_ld();
-                const int valid = min(kBN, kend - (kbeg + i * kBN));
                 if (valid < kBN) {
 #pragma unroll
                     for (int j = 0; j < kBN; ++j)
                         if (j >= valid) sv[j] = __float_as_uint(-INFINITY);
                 }
-                // row max: 8 chains of 3-input max over 16 columns each
-                float mx8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float mu = fmaxf(__uint_as_float(sv[u]), __uint_as_float(sv[u + 8]));
-#pragma unroll
-                    for (int k = 2; k < 16; k += 2)
-                        mu = ptx::fmax3(mu, __uint_as_float(sv[u + 8 * k]), __uint_as_float(sv[u + 8 * k + 8]));
-                    mx8[u] = mu;
-                }
-                const float mx = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
-                                       fmaxf(ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                const float m_blk = mx * c;
                 if (i == 0) {
-                    m = m_blk;
-                } else {
-                    const bool need = m_blk > m + kRescaleThreshold;
-                    if (__any_sync(kFullMask, need)) {
-                        // O (and l) carry the old maximum: rescale them in TMEM
-                        const float f = need ? ptx::ex2(m - m_blk) : 1.f;
+                    // the first block sets the running maximum: 3-input max over 8 chains
+                    float mx8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float mu = fmaxf(__uint_as_float(sv[u]), __uint_as_float(sv[u + 8]));
+#pragma unroll
+                        for (int k = 2; k < 16; k += 2)
+                            mu = ptx::fmax3(mu, __uint_as_float(sv[u + 8 * k]), __uint_as_float(sv[u + 8 * k + 8]));
+                        mx8[u] = mu;
+                    }
+                    m = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                              fmaxf(ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+                }
+                // p = 2^(s*c - m) against the running maximum m, with the block's own
+                // maximum tracked in the same pass (off the exp2 dependency chain).
+                // A row whose maximum grew by more than 2^8 has its O and l rescaled
+                // in TMEM and the pass redone; after the first block this is rare.
+                // Packed scale-and-subtract, exp2 on the MUFU unit (or the FMA-pipe
+                // cubic for kPolyPairs of every 8 pairs), packed row sums, and bf16
+                // pairs stored over the first 64 S columns as P for the PV MMA.
+                float blk = 0.f;
 #pragma unroll 1
-                        for (int q4 = 0; q4 < D / 16; ++q4) {
-                            uint32_t ov[16];
-                            ptx::tmem_ld16(tO + 16 * q4, ov);
-                            ptx::tmem_wait_ld();
+                for (int pass = 0;; ++pass) {
+                    const float neg_m = -m;
+                    float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
+                    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-                            ptx::tmem_st16(tO + 16 * q4, ov);
+                    for (int qtr = 0; qtr < 4; ++qtr) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = 32 * qtr + 2 * j;
+                            const float s0 = __uint_as_float(sv[col]), s1 = __uint_as_float(sv[col + 1]);
+                            float x0, x1, p0, p1;
+                            ptx::ffma2(x0, x1, s0, s1, c, c, neg_m, neg_m);
+                            mq[j & 3] = ptx::fmax3(mq[j & 3], s0, s1);
+                            if ((j & 7) < kPolyPairs) {
+                                ptx::ex2_poly2(x0, x1, p0, p1);
+                            } else {
+                                p0 = ptx::ex2(x0);
+                                p1 = ptx::ex2(x1);
+                            }
+                            ptx::fadd2(sa[j & 1], sb[j & 1], sa[j & 1], sb[j & 1], p0, p1);
+                            pk[j] = pack_bf16x2(p0, p1);
                         }
-                        ptx::tmem_wait_st();
-                        l *= f;
-                        if (need) m = m_blk;
+                        ptx::tmem_st16(tS + 16 * qtr, pk);
                     }
-                }
-                // p = 2^(s*c - m): packed scale-and-subtract, then exp2 on the MUFU
-                // unit for most pairs and on the FMA pipe (cubic) for kPolyPairs of
-                // every 8, to balance the two pipes; packed row sums; bf16 pairs
-                // stored over the first 64 S columns as P for the PV MMA
-                const float neg_m = -m;
-                float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
+                    blk = (sa[0] + sa[1]) + (sb[0] + sb[1]);
+                    const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c;
+                    const bool need = m_blk > m + kRescaleThreshold;
+                    if (!__any_sync(kFullMask, need)) break;
+                    // O (and l) carry the old maximum: rescale them in TMEM, then redo
+                    const float f = need ? ptx::ex2(m - m_blk) : 1.f;
+#pragma unroll 1
+                    for (int q4 = 0; q4 < D / 16; ++q4) {
+                        uint32_t ov[16];
+                        ptx::tmem_ld16(tO + 16 * q4, ov);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                for (int qtr = 0; qtr < 4; ++qtr) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 32 * qtr + 2 * j;
-                        float x0, x1, p0, p1;
-                        ptx::ffma2(x0, x1, __uint_as_float(sv[col]), __uint_as_float(sv[col + 1]), c, c, neg_m,
-                                   neg_m);
-                        if ((j & 7) < kPolyPairs) {
-                            ptx::ex2_poly2(x0, x1, p0, p1);
-                        } else {
-                            p0 = ptx::ex2(x0);
-                            p1 = ptx::ex2(x1);
-                        }
-                        ptx::fadd2(sa[j & 1], sb[j & 1], sa[j & 1], sb[j & 1], p0, p1);
-                        pk[j] = pack_bf16x2(p0, p1);
+                        for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
+                        ptx::tmem_st16(tO + 16 * q4, ov);
                     }
-                    ptx::tmem_st16(tS + 16 * qtr, pk);
+                    l *= f;
+                    if (need) m = m_blk;
                 }
-                l += (sa[0] + sa[1]) + (sb[0] + sb[1]);
+                l += blk;
                 // P is in TMEM: each thread's stores complete and are fenced, the
                 // warp synchronises, and one lane signals for the warp
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
+                if (!kv_seen) {
+                    ok = wait_lane(v_bar(), v_par(), abort_flag);
+                    if (ok && i + 1 < nb) ok = wait_lane(bar(kBarKvFull + nk % kStages), (nk / kStages) & 1, abort_flag);
+                }
+                if (!__all_sync(kFullMask, ok)) {
+                    ok = false;
+                    break;
+                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kBarPFull + t));
             }
@@ -594,7 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row_valid();
         const long long row = row_index();
         if (tile_active && p.a.fused) {
-            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx);
+            // the beam warps have filled the chain tables
+            const bool beam_ok = wait_warp(bar(kBarBeam), 0, abort_flag);
+            if (!beam_ok) fail();
+            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx, beam_ok);
         } else if (tile_active) {
             const long long n_rows = (long long)g.R * g.W_s * g.Hq;
             float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
@@ -699,7 +814,7 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
 }  // namespace
 
 int tc_beams_per_tile(int G) { return kBM / G; }
-int tc_fused_max_steps() { return kFusedMaxTokens; }
+int tc_fused_max_steps(int) { return kFusedMaxTokens; }
 
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s) {
     const int bpt = tc_beams_per_tile(a.g.G);

@@ -186,7 +186,7 @@ struct Layout {
 // shared-memory scratch), the tensor-core kernel runs the per-beam stage and
 // the merge itself: no partials, no workspace, one kernel.
 bool fused_merge(const Geometry &g, const SplitPlan &p) {
-    return chosen_path() == Path::kTensorCore && p.n_splits == 1 && g.step < tc_fused_max_steps();
+    return chosen_path() == Path::kTensorCore && p.n_splits == 1 && g.step < tc_fused_max_steps(g.G);
 }
 
 Layout workspace_layout(const Geometry &g, const SplitPlan &p) {

@@ -76,7 +76,7 @@ cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
 
 // gr_ctx_tc.cu  (tensor-core context stage)
 int tc_beams_per_tile(int G);
-int tc_fused_max_steps();  // the fused epilogue holds chains of steps < this
+int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 
 }  // namespace gr
