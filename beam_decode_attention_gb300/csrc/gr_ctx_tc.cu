@@ -45,7 +45,10 @@ constexpr int kMmaWarp = 9;
 constexpr int kBeamWarp = 10;               // warps 10 and 11: per-beam stage
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// A block whose p = 2^(s*c - m) sum past this (so some p may be past it) has
+// its row rescaled; below it every p is bounded by it, far from the fp32 and
+// bf16 ranges, so the running maximum may lag the true one by up to 16 (log2)
+constexpr float kSumLimit = 65536.0f;
 constexpr int kFusedMaxTokens = 8;          // chain tokens the fused epilogue holds (steps < 8)
 // of every 8 column pairs, how many take exp2 from the FMA-pipe cubic instead
 // of the MUFU unit; on GB300 (ex2 at 32 lanes/clock/SM) all-MUFU measured fastest
@@ -507,14 +510,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // A thread that has just issued MMAs stalls on its next mbarrier
             // wait until they have drained into the tensor pipe, which then runs
-            // dry: every wait here costs pipe time.  So the issuer waits only for
-            // P; the softmax warps certify, before they signal P_t(i), that V(i)
-            // and K(i+1) have landed.
+            // dry: every wait here costs pipe time, but back-to-back waits cost
+            // little more than one.  So the issuer waits at two points per
+            // block: for P_0(i) together with V(i) and K(i+1), and for P_1(i).
             for (int i = 0; ok && i < nb; ++i) {
                 const int sv = (2 * i + 1) % kStages;
                 const bool has_next = (i + 1) < nb;
                 const int sk = (2 * (i + 1)) % kStages;
                 if (!(ok = wait_lane(bar(kBarPFull + 0), i & 1, abort_flag))) break;
+                {
+                    // a tail block's V is usable once the producer has zeroed its rows past the end
+                    const int valid = min(kBN, kend - (kbeg + i * kBN));
+                    const int nv = 2 * i + 1, nk = 2 * (i + 1);
+                    if (!(ok = (valid < kBN) ? wait_lane(bar(kBarVTail), 0, abort_flag)
+                                             : wait_lane(bar(kBarKvFull + nv % kStages), (nv / kStages) & 1, abort_flag)))
+                        break;
+                    if (has_next && !(ok = wait_lane(bar(kBarKvFull + nk % kStages), (nk / kStages) & 1, abort_flag))) break;
+                }
                 issue_pv(0, sv, i);
                 if (i == nb - 1) ptx::mma_commit(bar(kBarODone + 0));
                 if (has_next) issue_s(0, sk);
@@ -538,8 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kBeamWarp) {
         // ------------------------------------------------------------ per-beam stage
-        // 64 threads, four rows each (rows b and b + 64 of each tile, two at a
-        // time), while the context loop runs; then one arrival per warp.
+        // 64 threads, four rows each (rows b and b + 64 of each tile, one at a
+        // time: measured faster than two rows in flight, which load the SM's
+        // memory pipeline harder while the softmax warps use it), while the
+        // context loop runs; then one arrival per warp.
         if (p.a.fused) {
             bool okq = nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag);   // q is read from the Q tile
             if (!okq) {
@@ -551,19 +565,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = (warp - kBeamWarp) * 32 + lane;
                 for (int t = 0; t < 2; ++t) {
                     if (t == 1 && !t1_active) break;
-                    BeamRow br[2];
-#pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         const int m_local = b + 64 * k;
                         const int beam = (tile0 + t) * p.bpt + m_local / g.G;
-                        br[k].valid = (m_local < rows_per_tile) && (beam < g.W_s);
-                        br[k].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
-                        br[k].beam = beam;
-                        br[k].ridx = t * kBM + m_local;
-                        br[k].q_smem = sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u;
-                        br[k].swz = m_local & 7;
+                        BeamRow br[1];
+                        br[0].valid = (m_local < rows_per_tile) && (beam < g.W_s);
+                        br[0].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
+                        br[0].beam = beam;
+                        br[0].ridx = t * kBM + m_local;
+                        br[0].q_smem = sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u;
+                        br[0].swz = m_local & 7;
+                        beam_prologue<D, 1>(p.a, r, kvh, br, nb > 0, s_x, s_slot, s_bad);
                     }
-                    beam_prologue<D, 2>(p.a, r, kvh, br, nb > 0, s_x, s_slot, s_bad);
                 }
             }
             __syncwarp();
@@ -593,18 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (tile_active && nb > 0) {
             for (int i = 0; i < nb; ++i) {
-                // P_t(i) also tells the issuer that V(i) and K(i+1) have landed (the
-                // issuer itself waits only for P).  One lane per tile looks while the
-                // warp would wait for S anyway, and waits after the pass only if a
-                // load was still in flight.
                 const int valid = min(kBN, kend - (kbeg + i * kBN));
-                const int nv = 2 * i + 1, nk = 2 * (i + 1);
-                auto v_bar = [&]() { return valid < kBN ? bar(kBarVTail) : bar(kBarKvFull + nv % kStages); };
-                auto v_par = [&]() -> uint32_t { return valid < kBN ? 0u : (uint32_t)((nv / kStages) & 1); };
-                bool kv_seen = true;
-                if (quarter == 0 && lane == 0)
-                    kv_seen = ptx::mbar_test_wait(v_bar(), v_par()) &&
-                              (i + 1 >= nb || ptx::mbar_test_wait(bar(kBarKvFull + nk % kStages), (nk / kStages) & 1));
                 if (!(ok = wait_warp(bar(kBarSFull + t), i & 1, abort_flag))) break;
                 ptx::tc_fence_after();
                 uint32_t sv[kBN];
@@ -631,19 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
                               fmaxf(ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
                 }
-                // p = 2^(s*c - m) against the running maximum m, with the block's own
-                // maximum tracked in the same pass (off the exp2 dependency chain).
-                // A row whose maximum grew by more than 2^8 has its O and l rescaled
-                // in TMEM and the pass redone; after the first block this is rare.
-                // Packed scale-and-subtract, exp2 on the MUFU unit (or the FMA-pipe
-                // cubic for kPolyPairs of every 8 pairs), packed row sums, and bf16
-                // pairs stored over the first 64 S columns as P for the PV MMA.
+                // p = 2^(s*c - m) against the running maximum m.  The block's own
+                // maximum is not computed: every p is at most the block's sum, so a
+                // sum of at most kSumLimit bounds every p and the row needs no
+                // rescale.  Past it (rare after the first block, or inf/NaN) the
+                // block maximum is taken from the scores still in registers, O and
+                // l are rescaled in TMEM and the pass is redone once.  Packed
+                // scale-and-subtract, exp2 on the MUFU unit (or the FMA-pipe cubic
+                // for kPolyPairs of every 8 pairs), packed row sums, and bf16 pairs
+                // stored over the first 64 S columns as P for the PV MMA.
                 float blk = 0.f;
 #pragma unroll 1
-                for (int pass = 0;; ++pass) {
+                for (int pass = 0; pass < 2; ++pass) {
                     const float neg_m = -m;
                     float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
-                    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int qtr = 0; qtr < 4; ++qtr) {
                         uint32_t pk[16];
@@ -653,7 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float s0 = __uint_as_float(sv[col]), s1 = __uint_as_float(sv[col + 1]);
                             float x0, x1, p0, p1;
                             ptx::ffma2(x0, x1, s0, s1, c, c, neg_m, neg_m);
-                            mq[j & 3] = ptx::fmax3(mq[j & 3], s0, s1);
                             if ((j & 7) < kPolyPairs) {
                                 ptx::ex2_poly2(x0, x1, p0, p1);
                             } else {
@@ -666,9 +668,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_st16(tS + 16 * qtr, pk);
                     }
                     blk = (sa[0] + sa[1]) + (sb[0] + sb[1]);
-                    const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c;
-                    const bool need = m_blk > m + kRescaleThreshold;
+                    const bool need = pass == 0 && !(blk <= kSumLimit);
                     if (!__any_sync(kFullMask, need)) break;
+                    float mx8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float mu = fmaxf(__uint_as_float(sv[u]), __uint_as_float(sv[u + 8]));
+#pragma unroll
+                        for (int k = 2; k < 16; k += 2)
+                            mu = ptx::fmax3(mu, __uint_as_float(sv[u + 8 * k]), __uint_as_float(sv[u + 8 * k + 8]));
+                        mx8[u] = mu;
+                    }
+                    const float m_blk = fmaxf(ptx::fmax3(mx8[0], mx8[1], mx8[2]),
+                                              fmaxf(ptx::fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
                     // O (and l) carry the old maximum: rescale them in TMEM, then redo
                     const float f = need ? ptx::ex2(m - m_blk) : 1.f;
 #pragma unroll 1
@@ -688,14 +700,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // warp synchronises, and one lane signals for the warp
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                if (!kv_seen) {
-                    ok = wait_lane(v_bar(), v_par(), abort_flag);
-                    if (ok && i + 1 < nb) ok = wait_lane(bar(kBarKvFull + nk % kStages), (nk / kStages) & 1, abort_flag);
-                }
-                if (!__all_sync(kFullMask, ok)) {
-                    ok = false;
-                    break;
-                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(kBarPFull + t));
             }

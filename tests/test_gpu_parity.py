@@ -147,6 +147,26 @@ def test_tagged_beam_values():
         compare(out, lse, ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("jump", [3.0, 40.0])
+def test_running_max_jumps(jump):
+    """Context keys past position 300 are scaled up so that the scores of
+    later key blocks exceed the running maximum by far (x3: the block sums
+    pass the rescale limit; x40: exp2 overflows to inf before the rescale),
+    and the first keys are scaled down: the online softmax must rescale O and
+    l and redo the block, in either key split.  V is scaled by 1/4 (exact in
+    bf16): such peaked weights make out nearly one V row, and with |v| up to
+    ~4 the bf16 rounding of P and of out alone approaches the 1e-2 gate."""
+    inp = workloads.make_custom(2, 16, 8, 128, [700, 1000], [4, 6, 9], seed=83, q_scale=2.0)
+    k = workloads.bf16_bits_to_f32(inp["ctx_k"])
+    k[:, :, 300:] *= jump
+    k[:, :, :60] *= 0.25
+    inp["ctx_k"] = workloads.f32_to_bf16_bits(k)
+    for key in ("ctx_v", "beam_v"):
+        inp[key] = workloads.f32_to_bf16_bits(workloads.bf16_bits_to_f32(inp[key]) * 0.25)
+    for splits in (1, 2):
+        _run_custom(inp, steps=[0, 2], splits=splits)
+
+
 def test_repeatable_and_stream():
     inp = workloads.make_custom(2, 16, 8, 128, [333, 64], [8, 20, 30], seed=71)
     dev = DeviceWorkload(inp)
