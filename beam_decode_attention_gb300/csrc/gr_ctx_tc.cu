@@ -228,19 +228,22 @@ __device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, 
 // Merge for the row this thread owns (fused epilogue, single key split): the
 // context partial (O in TMEM, running max m in base-2 units, sum l) and the
 // chain tokens scored by beam_prologue are combined by log-sum-exp (the
-// merging stage), and the final bf16 row and fp32 LSE are written.  The
-// chain's V rows were prefetched into L2 by the beam warps; they are loaded
-// two tokens at a time.  tcgen05.ld is warp-collective, so every lane takes
-// part in the O loads.  beam_ok is false when the beam warps gave up (the
-// call already reports a timeout): the row is then written as NaN without
-// reading the chain tables.
+// merging stage); the fp32 LSE is written, and the final bf16 row goes into
+// `stage` (the tile's Q tile: row m_local, 128-byte swizzled as TMA lays it
+// out) for the tile's TMA store.  The chain's V rows were prefetched into L2
+// by the beam warps; they are loaded two tokens at a time.  tcgen05.ld is
+// warp-collective, so every lane takes part in the O loads.  beam_ok is false
+// when the beam warps gave up (the call already reports a timeout): the row
+// is then written as NaN without reading the chain tables.
 template <int D>
 __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, long long row, bool row_ok,
                                               bool have_ctx, float m_ctx, float l_ctx, uint32_t tO,
                                               const float *s_x, const int *s_slot, const int *s_bad, int ridx,
-                                              bool beam_ok) {
+                                              bool beam_ok, uint32_t stage, int m_local) {
     const Geometry &g = a.g;
-    uint16_t *orow = a.out + row * D;
+    auto stage_chunk = [&](int hh, int c) -> uint32_t {
+        return stage + (uint32_t)(hh * (kBM * 128) + m_local * 128 + ((c ^ (m_local & 7)) << 4));
+    };
     const bool bad = row_ok && (!beam_ok || s_bad[ridx] != 0);
     if (!have_ctx) {
         m_ctx = -INFINITY;
@@ -265,7 +268,15 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
 #pragma unroll
             for (int d = 0; d < 64; ++d) acc[d] = 0.f;
         }
-        if (!row_ok || bad) continue;
+        if (!row_ok) continue;
+        if (bad) {
+            // NaN marks a row whose chain is broken
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(stage_chunk(hh, c)), "r"(0x7fc07fc0u)
+                             : "memory");
+            continue;
+        }
         const float wc = w_ctx * inv;
 #pragma unroll
         for (int d = 0; d < 64; ++d) acc[d] *= wc;
@@ -304,18 +315,15 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
                 }
             }
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + 64 * hh);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                                pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage_chunk(hh, c)),
+                         "r"(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1])), "r"(pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3])),
+                         "r"(pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5])), "r"(pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]))
+                         : "memory");
     }
     if (!row_ok) return;
     if (bad) {
-        // NaN marks a row whose chain is broken
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c)
-            reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
         a.lse[row] = __int_as_float(0x7fc00000);
         if (beam_ok) raise_device_error(a.err, kDevErrBadParent);
         return;
@@ -326,7 +334,8 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ TcParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                  const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -713,7 +722,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the beam warps have filled the chain tables
             const bool beam_ok = wait_warp(bar(kBarBeam), 0, abort_flag);
             if (!beam_ok) fail();
-            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx, beam_ok);
+            // the final rows leave through this tile's Q tile (free: every S of
+            // the tile has completed, the beam warps are done with q) by TMA
+            const uint32_t stage = sbase + C::kQOff + t * C::kTileBytes;
+            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx, beam_ok, stage,
+                             m_local);
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(1 + t, 4 * 32);
+            if (quarter == 0 && lane == 0) {
+                for (int h = 0; h < C::kHalves; ++h)
+                    ptx::tma_store_4d(&tm_out, stage + h * C::kHalfBytes, h * 64, kvh * g.G, (tile0 + t) * p.bpt, r);
+                ptx::bulk_commit();
+                ptx::bulk_wait_all();   // the rows are written before the CTA (and its shared memory) ends
+            }
         } else if (tile_active) {
             const long long n_rows = (long long)g.R * g.W_s * g.Hq;
             float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
@@ -796,7 +817,7 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
         }
     }
     const Geometry &g = a.g;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t qd[4] = {(uint64_t)D, (uint64_t)g.Hq, (uint64_t)g.W_s, (uint64_t)g.R};
     const uint64_t qs[3] = {(uint64_t)D * 2, (uint64_t)g.Hq * D * 2, (uint64_t)g.W_s * g.Hq * D * 2};
     const uint32_t qb[4] = {64, (uint32_t)g.G, (uint32_t)bpt, 1};
@@ -811,7 +832,13 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
     p.bpt = bpt;
     p.tiles = tiles;
     dim3 grid((tiles + 1) / 2, g.R * g.Hkv, a.sp.n_splits);
-    ctx_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, p);
+    // fused path: the output rows leave by TMA stores with the Q tiles' geometry
+    if (a.fused) {
+        if (!encode_4d(&to, a.out, qd, qs, qb)) return cudaErrorInvalidValue;
+    } else {
+        to = tq;   // unused
+    }
+    ctx_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
