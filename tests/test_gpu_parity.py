@@ -116,6 +116,37 @@ def test_head_geometries(Hq, Hkv, D):
     _run_custom(inp)
 
 
+@pytest.mark.parametrize("lens", [[0, 300], [130, 1]])
+def test_two_chain_blocks_per_level(lens):
+    """One query head per kv head (G = 1) and up to 256 beams: a CTA of the
+    fused single-split path holds two 128-beam tiles, so its per-beam stage
+    walks 256 chains; with no context (ctx_len 0) the rows are the chain
+    tokens alone, and with one context key few tokens carry all the weight."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(2, 4, 4, 128, lens, [5, 140, 256], seed=sum(lens) + 11)
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = "1"
+    try:
+        assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)["fused_merge"] == 1
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+    _run_custom(inp, splits=1)
+
+
+def test_fused_chain_of_eight_levels():
+    """Steps 5 and 7 in one key split: chains of six and eight tokens, the
+    longest the fused single-split path takes."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(2, 16, 8, 128, [200, 90], [2, 3, 4, 5, 6, 7, 8, 9], seed=92)
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = "1"
+    try:
+        assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 7)["fused_merge"] == 1
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+    _run_custom(inp, steps=[5, 7], splits=1)
+
+
 def test_width_one():
     inp = workloads.make_custom(3, 16, 8, 128, [64, 500, 3], [1, 1, 1], seed=17)
     _run_custom(inp)
