@@ -12,6 +12,9 @@ The functions mirror the C entry points:
 * :func:`gr_decode_attn_workspace_size`;
 * :func:`gr_resolve_ancestors` / :func:`gr_validate_beam_path` -- BeamPath
   utilities;
+* :func:`gr_beam_select` / :func:`gr_beam_select_workspace_size` -- beam
+  selection after a decode forward (log_softmax + top-W over every beam's
+  logits, giving the next BeamPath row);
 * :func:`gr_get_device_error`, :func:`gr_status_string`.
 """
 
@@ -27,14 +30,19 @@ __all__ = [
     "GRError", "Shape", "load", "lib_path", "gr_decode_attn", "gr_decode_attn_workspace_size",
     "gr_resolve_ancestors", "gr_validate_beam_path", "gr_get_device_error", "gr_status_string",
     "gr_version", "EXPORTED_SYMBOLS", "gr_decode_attn_timed", "gr_decode_attn_plan", "PlanInfo",
-    "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES", "SelectShape", "gr_beam_select",
+    "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
 ]
 
 EXPORTED_SYMBOLS = (
     "gr_decode_attn_workspace_size", "gr_decode_attn", "gr_decode_attn_timed",
     "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
+    "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
 )
+
+# GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
+SELECT_MAX_WIDTH = 1024
 
 # bytes of the library's static scratch used by gr_decode_attn_noalloc
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -71,6 +79,16 @@ class Shape(ctypes.Structure):
         return cls(int(d["num_requests"]), int(d["num_q_heads"]), int(d["num_kv_heads"]),
                    int(d["head_dim"]), int(d["ctx_capacity"]), int(d["step_capacity"]),
                    int(d["beam_capacity"]), float(d["softmax_scale"]))
+
+
+class SelectShape(ctypes.Structure):
+    """``gr_select_shape``."""
+    _fields_ = [
+        ("num_requests", ctypes.c_int32),
+        ("width", ctypes.c_int32),
+        ("vocab", ctypes.c_int32),
+        ("next_width", ctypes.c_int32),
+    ]
 
 
 class PlanInfo(ctypes.Structure):
@@ -122,6 +140,13 @@ def load() -> ctypes.CDLL:
     lib.gr_resolve_ancestors.restype = ctypes.c_int
     lib.gr_validate_beam_path.argtypes = [sp, vp, vp, i32, vp, vp, vp]
     lib.gr_validate_beam_path.restype = ctypes.c_int
+    ssp = ctypes.POINTER(SelectShape)
+    lib.gr_beam_select_workspace_size.argtypes = [ssp]
+    lib.gr_beam_select_workspace_size.restype = sz
+    lib.gr_beam_select.argtypes = [ssp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, sz, vp]
+    lib.gr_beam_select.restype = ctypes.c_int
+    lib.gr_beam_select_timed.argtypes = [ssp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, sz, vp, vp]
+    lib.gr_beam_select_timed.restype = ctypes.c_int
     lib.gr_get_device_error.argtypes = []
     lib.gr_get_device_error.restype = ctypes.c_int
     lib.gr_status_string.argtypes = [ctypes.c_int]
@@ -244,6 +269,51 @@ def gr_validate_beam_path(shape: Shape, beam_path, widths: Sequence[int], step: 
                                       int(step), _ptr(ctx_len), _ptr(bad_count),
                                       _stream_handle(stream))
     _check(rc, "gr_validate_beam_path")
+
+
+def gr_beam_select_workspace_size(shape: SelectShape) -> int:
+    return int(load().gr_beam_select_workspace_size(ctypes.byref(shape)))
+
+
+def gr_beam_select(shape: SelectShape, logits, beam_scores, next_parent, next_token, next_score,
+                   workspace, parent_stride: Optional[int] = None,
+                   workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """Enqueue gr_beam_select on ``stream`` (default: torch's current stream).
+
+    ``logits`` fp32 [R, W_s, V], ``beam_scores`` fp32 [R, W_s]; writes
+    ``next_parent`` (row r at r * parent_stride, default next_width),
+    ``next_token`` and ``next_score`` ([R, next_width]).  Raises
+    :class:`GRError` on a non-zero status.
+    """
+    if parent_stride is None:
+        parent_stride = shape.next_width
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().gr_beam_select(ctypes.byref(shape), _ptr(logits), _ptr(beam_scores),
+                               _ptr(next_parent), int(parent_stride), _ptr(next_token),
+                               _ptr(next_score), _ptr(workspace), int(workspace_bytes),
+                               _stream_handle(stream))
+    _check(rc, "gr_beam_select")
+
+
+def gr_beam_select_timed(shape: SelectShape, logits, beam_scores, next_parent, next_token,
+                         next_score, workspace, events, parent_stride: Optional[int] = None,
+                         workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """gr_beam_select recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``)
+    before the per-row kernel, between the two kernels, and after the merge."""
+    if parent_stride is None:
+        parent_stride = shape.next_width
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    for e in events:
+        if e.cuda_event == 0:      # torch creates the event lazily on first record
+            e.record()
+    ev = (ctypes.c_void_p * 3)(*[int(e.cuda_event) for e in events])
+    rc = load().gr_beam_select_timed(ctypes.byref(shape), _ptr(logits), _ptr(beam_scores),
+                                     _ptr(next_parent), int(parent_stride), _ptr(next_token),
+                                     _ptr(next_score), _ptr(workspace), int(workspace_bytes),
+                                     _stream_handle(stream), ev)
+    _check(rc, "gr_beam_select_timed")
 
 
 def gr_get_device_error() -> int:

@@ -380,6 +380,57 @@ int gr_validate_beam_path(const gr_attn_shape *shape, const int32_t *beam_path, 
     return cuda_status(launch_validate(g, beam_path, ctx_len, bad_count, static_cast<cudaStream_t>(stream)));
 }
 
+size_t gr_beam_select_workspace_size(const gr_select_shape *shape) {
+    if (!shape || shape->num_requests < 1 || shape->width < 1 || shape->vocab < 1 || shape->next_width < 1 ||
+        shape->next_width > select_max_width() || (long long)shape->width * shape->vocab >= (1LL << 31) ||
+        shape->next_width > (long long)shape->width * shape->vocab)
+        return 0;
+    return select_list_bytes(shape->num_requests, shape->width, shape->vocab, shape->next_width);
+}
+
+static int beam_select_impl(const gr_select_shape *shape, const float *logits, const float *beam_scores,
+                            int32_t *next_parent, int64_t parent_stride, int32_t *next_token, float *next_score,
+                            void *workspace, size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events) {
+    if (!shape || !logits || !beam_scores || !next_parent || !next_token || !next_score || !workspace)
+        return GR_ERR_NULL_ARG;
+    const size_t need = gr_beam_select_workspace_size(shape);
+    if (need == 0 || parent_stride < shape->next_width) return GR_ERR_BAD_SHAPE;
+    if (misaligned(logits) || misaligned(beam_scores) || misaligned(next_parent) || misaligned(next_token) ||
+        misaligned(next_score) || misaligned(workspace))
+        return GR_ERR_MISALIGNED;
+    if (workspace_bytes < need) return GR_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo dev;
+    const int rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (events) {
+        if (!events[0] || !events[1] || !events[2]) return GR_ERR_NULL_ARG;
+        const int e0 = cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(events[0]), s));
+        if (e0 != GR_OK) return e0;
+    }
+    const int e1 = cuda_status(launch_beam_select(
+        shape->num_requests, shape->width, shape->vocab, shape->next_width, logits, beam_scores, next_parent,
+        (long long)parent_stride, next_token, next_score, workspace, s,
+        events ? static_cast<cudaEvent_t>(events[1]) : nullptr));
+    if (e1 != GR_OK || !events) return e1;
+    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(events[2]), s));
+}
+
+int gr_beam_select(const gr_select_shape *shape, const float *logits, const float *beam_scores,
+                   int32_t *next_parent, int64_t parent_stride, int32_t *next_token, float *next_score,
+                   void *workspace, size_t workspace_bytes, gr_stream_t stream) {
+    return beam_select_impl(shape, logits, beam_scores, next_parent, parent_stride, next_token, next_score,
+                            workspace, workspace_bytes, stream, nullptr);
+}
+
+int gr_beam_select_timed(const gr_select_shape *shape, const float *logits, const float *beam_scores,
+                         int32_t *next_parent, int64_t parent_stride, int32_t *next_token, float *next_score,
+                         void *workspace, size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events) {
+    if (!events) return GR_ERR_NULL_ARG;
+    return beam_select_impl(shape, logits, beam_scores, next_parent, parent_stride, next_token, next_score,
+                            workspace, workspace_bytes, stream, events);
+}
+
 int gr_get_device_error(void) {
     DeviceInfo dev;
     int rc = device_info(&dev);

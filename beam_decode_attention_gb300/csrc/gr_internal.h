@@ -79,4 +79,13 @@ int tc_beams_per_tile(int G);
 int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 
+// gr_select.cu  (beam selection)
+size_t select_list_bytes(int R, int W, int V, int next_width);
+int select_max_width();
+// `between` (may be null) is recorded on `s` between the two kernels
+cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float *logits,
+                               const float *beam_scores, int32_t *next_parent, long long parent_stride,
+                               int32_t *next_token, float *next_score, void *workspace, cudaStream_t s,
+                               cudaEvent_t between = nullptr);
+
 }  // namespace gr

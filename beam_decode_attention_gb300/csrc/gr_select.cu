@@ -1,0 +1,477 @@
+// gr_select.cu -- beam selection after a decode forward: log_softmax over
+// every active beam's logits, plus the beam's cumulative score, and the W'
+// best candidates of each request (SID-GR README, section 10 "TODO and
+// Roadmap": log_softmax + topK + beam selection on the device; xGR review,
+// "xBeam": one size-BW selection over all beams' candidates).
+//
+//   score[r, b, v] = S[r, b] + (z[r, b, v] - (m_b + ln sum_v exp(z[r, b, v] - m_b)))
+//
+// in fp32; candidates are ordered by score descending, then by the flat
+// index b * V + v ascending, and the first W' of each request give the next
+// BeamPath row (parents), the tokens and the new cumulative scores.
+//
+// Kernel 1 (select_rows_kernel), one CTA per beam row, grid-strided over the
+// rows with one CTA per SM, so that a row re-read right after its first pass
+// still sits in L2:
+//   pass 0 (HBM)  the row's maximum and sum of exponentials, and a 4096-bin
+//                 histogram of the logits' ordered bit patterns (top 12 bits);
+//                 the bin holding the row's L-th largest logit (L = min(W', V))
+//                 bounds the candidates the row can contribute;
+//   pass 1 (L2)   every logit at or above that bin (less a margin of a few
+//                 ulps, so that candidates whose rounded scores tie with the
+//                 bin's are kept) is scored and collected in shared memory,
+//                 sorted by (score desc, v asc), and the row's best L go to
+//                 the workspace.
+//   A row whose boundary bin holds more than the shared-memory capacity
+//   (ties, peaked or degenerate logits) takes an exact radix select on the
+//   scores instead (more passes, same result).
+// Kernel 2 (select_merge_kernel), one CTA per request: the W'-th largest
+// score over the sorted row lists by bisection on the ordered key, the
+// candidates above it plus the tied ones in flat-index order, and a final
+// sort by (score desc, flat index asc).
+#include <cstdint>
+#include <mutex>
+
+#include "gr_common.cuh"
+#include "gr_internal.h"
+
+namespace gr {
+
+namespace {
+
+constexpr int kRowThreads = 512;
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kCap = 4096;            // candidate slots per row in shared memory
+constexpr int kMergeThreads = 1024;
+constexpr int kMaxSel = 1024;         // GR_SELECT_MAX_WIDTH
+
+// Order-preserving map of an fp32 value to uint32 (-0 taken as +0).
+__device__ __forceinline__ uint32_t ord_key(float x) {
+    if (x == 0.f) x = 0.f;
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+struct RowArgs {
+    const float *logits;
+    const float *beam_scores;
+    unsigned long long *lists;   // [R * W_s][L] (score key << 32 | ~v), sorted descending
+    int rows, V, L;
+};
+
+// The fp32 score of logit z in a row with log-normaliser c and beam score S:
+// fl(S + fl(z - c)); monotone (non-decreasing) in z.
+__device__ __forceinline__ float score_of(float z, float c, float S) { return S + (z - c); }
+
+// Visit z = row[v] for v in [0, V): 16-byte loads where the row allows, in
+// groups of four per thread so that several loads are in flight.
+template <typename F>
+__device__ __forceinline__ void for_row(const float *row, int V, F &&f) {
+    const int head = min(V, (int)(((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15) >> 2));
+    for (int v = threadIdx.x; v < head; v += blockDim.x) f(__ldg(row + v), v);
+    const float4 *row4 = reinterpret_cast<const float4 *>(row + head);
+    const int n4 = (V - head) >> 2;
+    constexpr int kU = 4;
+    int i = threadIdx.x;
+    for (; i + (kU - 1) * (int)blockDim.x < n4; i += kU * blockDim.x) {
+        float4 x[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) x[u] = __ldg(row4 + i + u * blockDim.x);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int v = head + 4 * (i + u * blockDim.x);
+            f(x[u].x, v);
+            f(x[u].y, v + 1);
+            f(x[u].z, v + 2);
+            f(x[u].w, v + 3);
+        }
+    }
+    for (; i < n4; i += blockDim.x) {
+        const float4 x = __ldg(row4 + i);
+        const int v = head + 4 * i;
+        f(x.x, v);
+        f(x.y, v + 1);
+        f(x.z, v + 2);
+        f(x.w, v + 3);
+    }
+    for (int v = head + 4 * n4 + threadIdx.x; v < V; v += blockDim.x) f(__ldg(row + v), v);
+}
+
+// Online (max, sum of exp) pair; -inf logits add nothing.
+struct MaxSum {
+    float m, s;
+};
+__device__ __forceinline__ MaxSum ms_add(MaxSum a, float z) {
+    if (z == -INFINITY) return a;
+    if (z > a.m) {
+        a.s = a.s * __expf(a.m - z) + 1.f;   // a.m = -inf: 0 * ... = 0
+        a.m = z;
+    } else {
+        a.s += __expf(z - a.m);
+    }
+    return a;
+}
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
+    if (b.m == -INFINITY) return a;
+    if (a.m == -INFINITY) return b;
+    const float m = fmaxf(a.m, b.m);
+    return {m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
+}
+
+// Block-wide sum (all threads get it); `red` holds one int per warp.
+__device__ __forceinline__ int block_sum(int x, int *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFullMask, x, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    int t = 0;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    return t;
+}
+
+// Exclusive prefix sum over the block in thread order (all threads take part);
+// `red` holds one int per warp; returns the block total in *total.
+__device__ __forceinline__ int block_excl_scan(int x, int *red, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, inc, o);
+        if (lane >= o) inc += y;
+    }
+    __syncthreads();
+    if (lane == 31) red[warp] = inc;
+    __syncthreads();
+    int base = 0, tot = 0;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) base += red[w];
+        tot += red[w];
+    }
+    *total = tot;
+    return base + inc - x;
+}
+
+// Given a histogram (kHistBins counts, highest key bin last), the bin holding
+// the need-th largest element and the count of elements in higher bins.
+// Each thread owns kHistBins / blockDim consecutive bins.
+__device__ __forceinline__ void find_bin(const int *hist, int need, int *red, int *s_bin, int *s_above) {
+    const int per = kHistBins / blockDim.x;
+    const int hi = kHistBins - 1 - threadIdx.x * per;   // this thread's bins: hi, hi-1, ..., hi-per+1
+    int mine = 0;
+    for (int k = 0; k < per; ++k) mine += hist[hi - k];
+    int total;
+    const int above = block_excl_scan(mine, red, &total);   // elements in higher bins than this thread's
+    if (above < need && above + mine >= need) {
+        int acc = above;
+        for (int k = 0; k < per; ++k) {
+            const int c = hist[hi - k];
+            if (acc + c >= need) {
+                *s_bin = hi - k;
+                *s_above = acc;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
+// Descending bitonic sort of n (a power of two) 64-bit values in shared memory.
+__device__ __forceinline__ void bitonic_desc(unsigned long long *a, int n) {
+    for (int k = 2; k <= n; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const unsigned long long x = a[i], y = a[p];
+                    if (((i & k) == 0) ? (x < y) : (x > y)) {
+                        a[i] = y;
+                        a[p] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+__device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t low) {
+    return ((unsigned long long)key << 32) | low;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) {
+    extern __shared__ unsigned long long sel_smem[];
+    unsigned long long *cand = sel_smem;                          // [kCap]
+    int *hist = reinterpret_cast<int *>(cand + kCap);             // [kHistBins]
+    int *red = hist + kHistBins;                                  // [32]
+    __shared__ MaxSum s_ms[kRowThreads / 32];
+    __shared__ int s_bin, s_above, s_cnt;
+    __shared__ float s_c;
+
+    for (int row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const float *z = a.logits + (long long)row * a.V;
+        const float S = a.beam_scores[row];
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+
+        // pass 0: maximum, sum of exponentials, histogram of the logits' keys
+        MaxSum ms{-INFINITY, 0.f};
+        for_row(z, a.V, [&](float x, int) {
+            ms = ms_add(ms, x);
+            atomicAdd(&hist[ord_key(x) >> (32 - kHistBits)], 1);
+        });
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
+            ms = ms_merge(ms, other);
+        }
+        if ((threadIdx.x & 31) == 0) s_ms[threadIdx.x >> 5] = ms;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            MaxSum t = s_ms[0];
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
+            s_c = t.m + __logf(t.s);   // log-normaliser c_b
+            s_cnt = 0;
+        }
+        find_bin(hist, a.L, red, &s_bin, &s_above);
+        const float c = s_c;
+
+        // pass 1: candidates at or above the boundary bin, less a margin that
+        // keeps every logit whose rounded score could tie with the bin's
+        const float zlo = key_float((uint32_t)s_bin << (32 - kHistBits));
+        const float margin = (fabsf(c) + fabsf(S) + fabsf(zlo) + 1.f) * 0x1p-19f;
+        // a boundary bin below -inf (W' past the row's finite logits) decodes to
+        // a NaN pattern: then every logit is a candidate
+        const float zthr = zlo >= -3.402823466e38f ? zlo - margin : -INFINITY;
+        for_row(z, a.V, [&](float x, int v) {
+            if (x >= zthr) {
+                const int slot = atomicAdd(&s_cnt, 1);
+                if (slot < kCap) cand[slot] = pack(ord_key(score_of(x, c, S)), ~(uint32_t)v);
+            }
+        });
+        __syncthreads();
+        int n = s_cnt;
+        if (n > kCap) {
+            // Exact radix select of the L-th largest score key (12 + 12 + 8
+            // bits), then every larger score plus the tied ones in v order.
+            uint32_t prefix = 0, mask = 0;
+            int need = a.L;
+            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+            for (int rd = 0; rd < 3; ++rd) {
+                for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+                __syncthreads();
+                const int sh = shifts[rd];
+                const uint32_t bm = (1u << widths[rd]) - 1u;
+                for_row(z, a.V, [&](float x, int) {
+                    const uint32_t k = ord_key(score_of(x, c, S));
+                    // bins are placed at the top of the histogram so find_bin's
+                    // highest-first walk works for 8-bit rounds too
+                    if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
+                });
+                __syncthreads();
+                find_bin(hist, need, red, &s_bin, &s_above);
+                const uint32_t digit = bm - (uint32_t)(kHistBins - 1 - s_bin);
+                need -= s_above;
+                prefix |= digit << sh;
+                mask |= bm << sh;
+                __syncthreads();
+            }
+            const uint32_t kstar = prefix;
+            if (threadIdx.x == 0) s_cnt = 0;
+            __syncthreads();
+            // larger keys (fewer than L) in any order; ties in ascending v,
+            // chunk by chunk so that the order is kept
+            int taken = 0;
+            for (int base = 0; base < a.V; base += blockDim.x) {
+                const int v = base + threadIdx.x;
+                const float x = v < a.V ? __ldg(z + v) : -INFINITY;
+                const uint32_t k = v < a.V ? ord_key(score_of(x, c, S)) : 0u;
+                if (v < a.V && k > kstar) {
+                    const int slot = atomicAdd(&s_cnt, 1);
+                    if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
+                }
+                const int tie = (v < a.V && k == kstar) ? 1 : 0;
+                int tot;
+                const int rank = block_excl_scan(tie, red, &tot);
+                if (tie && taken + rank < need) {
+                    const int slot = atomicAdd(&s_cnt, 1);
+                    if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
+                }
+                taken += tot;
+                if (taken >= need) {
+                    // the remaining larger keys still have to be gathered
+                    for (int v2 = base + blockDim.x + threadIdx.x; v2 < a.V; v2 += blockDim.x) {
+                        const uint32_t k2 = ord_key(score_of(__ldg(z + v2), c, S));
+                        if (k2 > kstar) {
+                            const int slot = atomicAdd(&s_cnt, 1);
+                            if (slot < kCap) cand[slot] = pack(k2, ~(uint32_t)v2);
+                        }
+                    }
+                    break;
+                }
+            }
+            __syncthreads();
+            n = min(s_cnt, kCap);
+        }
+        int np2 = 1;
+        while (np2 < n) np2 <<= 1;
+        for (int i = n + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
+        __syncthreads();
+        bitonic_desc(cand, np2);
+        unsigned long long *out = a.lists + (long long)row * a.L;
+        for (int j = threadIdx.x; j < a.L; j += blockDim.x) out[j] = cand[j];
+        __syncthreads();
+    }
+}
+
+struct MergeSelArgs {
+    const unsigned long long *lists;
+    int W, V, L, next_width;
+    int32_t *next_parent;
+    long long parent_stride;
+    int32_t *next_token;
+    float *next_score;
+};
+
+// number of entries of a descending list (key in the high 32 bits) with key >= t
+__device__ __forceinline__ int count_ge(const unsigned long long *lst, int L, uint32_t t) {
+    int lo = 0, hi = L;   // first index whose key < t
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((uint32_t)(lst[mid] >> 32) >= t) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSelArgs a) {
+    __shared__ unsigned long long sel[kMaxSel];
+    __shared__ int red[32];
+    const int r = blockIdx.x;
+    const unsigned long long *lists = a.lists + (long long)r * a.W * a.L;
+    // lists b in [b0, b1) belong to this thread (consecutive, for in-order prefixes)
+    const int per = (a.W + blockDim.x - 1) / blockDim.x;
+    const int b0 = min(a.W, (int)threadIdx.x * per), b1 = min(a.W, b0 + per);
+    auto count_all = [&](uint32_t t) {
+        int c = 0;
+        for (int b = b0; b < b1; ++b) c += count_ge(lists + (long long)b * a.L, a.L, t);
+        return block_sum(c, red);
+    };
+    // tau = the largest key t with at least next_width entries >= t
+    uint32_t lo = 0u, hi = 0xffffffffu;
+    while (lo < hi) {
+        const uint32_t mid = lo + (uint32_t)(((unsigned long long)hi - lo + 1ull) >> 1);
+        if (count_all(mid) >= a.next_width) lo = mid;
+        else hi = mid - 1u;
+    }
+    const uint32_t tau = lo;
+    // per list: entries above tau (all taken) and tied with tau (taken in
+    // flat-index order: lists in b order, each list in v order)
+    int gt = 0, eq = 0;
+    for (int b = b0; b < b1; ++b) {
+        const unsigned long long *lst = lists + (long long)b * a.L;
+        const int ge = count_ge(lst, a.L, tau);
+        const int g = tau == 0xffffffffu ? 0 : count_ge(lst, a.L, tau + 1u);
+        gt += g;
+        eq += ge - g;
+    }
+    int n_gt, n_eq;
+    int pos_gt = block_excl_scan(gt, red, &n_gt);
+    int pos_eq = block_excl_scan(eq, red, &n_eq);
+    const int need = a.next_width - n_gt;
+    for (int b = b0; b < b1; ++b) {
+        const unsigned long long *lst = lists + (long long)b * a.L;
+        const int ge = count_ge(lst, a.L, tau);
+        const int g = tau == 0xffffffffu ? 0 : count_ge(lst, a.L, tau + 1u);
+        for (int j = 0; j < ge; ++j) {
+            const unsigned long long e = lst[j];
+            const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)e;
+            const unsigned long long item = ((e >> 32) << 32) | (uint32_t)~flat;
+            if (j < g) {
+                sel[pos_gt++] = item;
+            } else if (pos_eq < need) {
+                sel[n_gt + pos_eq] = item;
+                ++pos_eq;
+            }
+        }
+    }
+    __syncthreads();
+    int np2 = 1;
+    while (np2 < a.next_width) np2 <<= 1;
+    for (int i = a.next_width + threadIdx.x; i < np2; i += blockDim.x) sel[i] = 0ull;
+    __syncthreads();
+    bitonic_desc(sel, np2);
+    for (int j = threadIdx.x; j < a.next_width; j += blockDim.x) {
+        const unsigned long long e = sel[j];
+        const uint32_t flat = ~(uint32_t)e;
+        a.next_parent[(long long)r * a.parent_stride + j] = (int32_t)(flat / (uint32_t)a.V);
+        a.next_token[(long long)r * a.next_width + j] = (int32_t)(flat % (uint32_t)a.V);
+        a.next_score[(long long)r * a.next_width + j] = key_float((uint32_t)(e >> 32));
+    }
+}
+
+}  // namespace
+
+size_t select_list_bytes(int R, int W, int V, int next_width) {
+    const long long L = next_width < V ? next_width : V;
+    return (size_t)R * W * L * sizeof(unsigned long long);
+}
+
+int select_max_width() { return kMaxSel; }
+
+cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float *logits,
+                               const float *beam_scores, int32_t *next_parent, long long parent_stride,
+                               int32_t *next_token, float *next_score, void *workspace, cudaStream_t s,
+                               cudaEvent_t between) {
+    static std::mutex mu;
+    static int sm_count[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (sm_count[dev] == 0) {
+            int n = 0;
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kCap * 8 + kHistBins * 4 + 32 * 4);
+            if (e != cudaSuccess) return e;
+            sm_count[dev] = n;
+        }
+    }
+    RowArgs ra;
+    ra.logits = logits;
+    ra.beam_scores = beam_scores;
+    ra.lists = static_cast<unsigned long long *>(workspace);
+    ra.rows = R * W;
+    ra.V = V;
+    ra.L = next_width < V ? next_width : V;
+    const int smem = kCap * 8 + kHistBins * 4 + 32 * 4;
+    const int grid = ra.rows < sm_count[dev] ? ra.rows : sm_count[dev];
+    select_rows_kernel<<<grid, kRowThreads, smem, s>>>(ra);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && between) e = cudaEventRecord(between, s);
+    if (e != cudaSuccess) return e;
+    MergeSelArgs ma;
+    ma.lists = ra.lists;
+    ma.W = W;
+    ma.V = V;
+    ma.L = ra.L;
+    ma.next_width = next_width;
+    ma.next_parent = next_parent;
+    ma.parent_stride = parent_stride;
+    ma.next_token = next_token;
+    ma.next_score = next_score;
+    select_merge_kernel<<<R, kMergeThreads, 0, s>>>(ma);
+    return cudaGetLastError();
+}
+
+}  // namespace gr

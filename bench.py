@@ -11,6 +11,12 @@ is flushed (a 2x-L2 buffer is written) before every timed call; the flush
 is outside the timed interval.
 
     python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+
+``--op beam_select`` measures the beam-selection step instead (log_softmax +
+top-W over every beam's logits, gr_beam_select): 4 requests, 900 -> 900
+beams, a 151,936-token vocabulary of fp32 logits (2.19 GB per call, larger
+than L2, so no flush is needed); its line carries the HBM roofline of the
+per-row kernel that reads the logits.
 """
 
 from __future__ import annotations
@@ -49,6 +55,7 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--op", choices=["attention", "beam_select"], default="attention")
     return p.parse_args()
 
 
@@ -253,11 +260,115 @@ def config_of(spec, inp):
             "l2": "flushed (2x L2 buffer written) before every timed call"}
 
 
+SELECT_METRIC = "µs per beam-selection call (R=4, W=900->900, V=151936, fp32 logits); % of HBM roofline"
+SELECT_UNIT = "us/call"
+
+
+def select_oracle_baseline(inp, next_width):
+    """The selection oracle on one request, scaled to the whole call."""
+    from oracle import select
+    R = inp["logits"].shape[0]
+    t0 = time.perf_counter()
+    select.top_candidates(inp["logits"][:1], inp["beam_scores"][:1], next_width)
+    dt = time.perf_counter() - t0
+    return dict(value=dt * R * 1e6, unit=SELECT_UNIT, cores=1, kind="oracle",
+                sample=f"request 0 of {R} (every beam and token of it), time scaled by {R}",
+                cpu_seconds=dt)
+
+
+def run_select_bench(args):
+    import torch
+    import beam_decode_attention_gb300 as gr
+    cfg = workloads.SELECT_HEADLINE
+    R, W, V, n = cfg["num_requests"], cfg["width"], cfg["vocab"], cfg["next_width"]
+    inp = workloads.make_select_inputs(R, W, V, seed=4242)
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        vals = [select_oracle_baseline(inp, n) for _ in range(max(1, min(args.steps, 3)))]
+        value = float(np.mean([v["value"] for v in vals]))
+        print(json.dumps({
+            "impl": "reference", "metric": SELECT_METRIC, "value": value, "unit": SELECT_UNIT, "n_gpus": 1,
+            "steps": len(vals), "warmup": 0, "ms_per_step": value / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "beam_select_r4_w900_v151936", **cfg},
+            "cpu_baseline": {"value": value, "unit": SELECT_UNIT, "cores": 1, "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": SELECT_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
+    torch.cuda.set_device(0)
+    gr.load()
+    stream = torch.cuda.current_stream()
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    scores = torch.from_numpy(inp["beam_scores"]).cuda()
+    shape = gr.SelectShape(R, W, V, n)
+    ws = torch.empty(gr.gr_beam_select_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    par = torch.empty((R, n), dtype=torch.int32, device="cuda")
+    tok = torch.empty((R, n), dtype=torch.int32, device="cuda")
+    sco = torch.empty((R, n), dtype=torch.float32, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        gr.gr_beam_select(shape, logits, scores, par, tok, sco, ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    call_us, rows_us = [], []
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        gr.gr_beam_select_timed(shape, logits, scores, par, tok, sco, ws, ev)
+        torch.cuda.synchronize()
+        call_us.append(ev[0].elapsed_time(ev[2]) * 1000.0)
+        rows_us.append(ev[0].elapsed_time(ev[1]) * 1000.0)
+    clk = clocks.stop()
+    value = float(np.mean(call_us))
+    pk = peaks()
+    logit_bytes = R * W * V * 4
+    alg_bytes = logit_bytes + R * W * 4 + R * n * 12     # logits and beam scores read once, outputs
+    achieved = alg_bytes / (float(np.mean(rows_us)) * 1e-6) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+        h_scores = torch.from_numpy(inp["beam_scores"]).pin_memory()
+        h_out = [torch.empty((R, n), dtype=d).pin_memory() for d in (torch.int32, torch.int32, torch.float32)]
+        times = []
+        for i in range(max(2, min(args.steps, 5)) + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            logits.copy_(h_logits, non_blocking=True)
+            scores.copy_(h_scores, non_blocking=True)
+            gr.gr_beam_select(shape, logits, scores, par, tok, sco, ws)
+            for h, d in zip(h_out, (par, tok, sco)):
+                h.copy_(d, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            if i > 0:
+                times.append(e0.elapsed_time(e1) * 1000.0)
+        e2e = {"value": float(np.mean(times)), "unit": SELECT_UNIT,
+               "h2d_bytes_per_step": logit_bytes + R * W * 4, "d2h_bytes_per_step": R * n * 12,
+               "note": "per call: logits and beam scores copied from pinned host memory, the three outputs back"}
+    cpu = None if args.no_cpu_baseline else select_oracle_baseline(inp, n)
+    line = {
+        "metric": SELECT_METRIC, "value": value, "unit": SELECT_UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": value / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "beam_select_r4_w900_v151936", **cfg,
+                   "l2": "inputs (2.19 GB of logits per call) larger than L2; no flush"},
+        "row_kernel_us": float(np.mean(rows_us)), "merge_kernel_us": float(np.mean(call_us) - np.mean(rows_us)),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 3), "traffic": None,
+                     "kernel": "select_rows_kernel", "peak_source": pk.get("source", "measured copy")},
+        "gpu_launches": 2 * args.steps, "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.gpus != 1:
         print(json.dumps({"error": "this build runs on one GPU; --gpus must be 1"}))
         return 2
+    if args.op == "beam_select":
+        return run_select_bench(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

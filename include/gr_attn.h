@@ -214,6 +214,69 @@ int gr_validate_beam_path(const gr_attn_shape *shape, const int32_t *beam_path,
  */
 int gr_get_device_error(void);
 
+/*
+ * Beam selection after a decode forward (SID-GR Inference README, section 10
+ * "TODO and Roadmap": log_softmax + topK + beam selection on the device;
+ * xGR review, "xBeam": one size-BW selection over every beam's candidates).
+ *
+ * For request r, active beam b < W_s with cumulative log-probability
+ * beam_scores[r, b] and next-token logits logits[r, b, 0 .. V-1]:
+ *     score[r, b, v] = beam_scores[r, b]
+ *                    + (logits[r, b, v] - (m_b + ln sum_v' exp(logits[r, b, v'] - m_b)))
+ * in fp32, m_b the row maximum.  The next_width candidates (b, v) of largest
+ * score are kept, equal scores ordered by the smaller flat index b * V + v,
+ * and written in that order:
+ *     next_parent[r * parent_stride + j] = b   (the next BeamPath row: pass
+ *                                               &beam_path[r0][s+1][0] with
+ *                                               parent_stride = S_max * W_max
+ *                                               to write it in place)
+ *     next_token [r * next_width + j]    = v
+ *     next_score [r * next_width + j]    = score[r, b, v]
+ * No length penalty or score normalisation is applied (the pages leave them
+ * open).  A logit of -inf masks its token; every beam needs at least one
+ * finite logit, and no logit may be NaN or +inf (not checked).
+ */
+#define GR_SELECT_MAX_WIDTH 1024
+
+typedef struct {
+    int32_t num_requests; /* R >= 1 */
+    int32_t width;        /* W_s >= 1: active beams per request */
+    int32_t vocab;        /* V >= 1: logits per beam; W_s * V < 2^31 */
+    int32_t next_width;   /* W': 1 <= W' <= min(GR_SELECT_MAX_WIDTH, W_s * V) */
+} gr_select_shape;
+
+/* Bytes of device workspace gr_beam_select needs (0 on a bad shape). */
+size_t gr_beam_select_workspace_size(const gr_select_shape *shape);
+
+/*
+ *   logits       device fp32 [R, W_s, V]
+ *   beam_scores  device fp32 [R, W_s]
+ *   next_parent  device int32, R rows of next_width entries, row r at
+ *                next_parent + r * parent_stride (parent_stride >= next_width)
+ *   next_token   device int32 [R, next_width], written
+ *   next_score   device fp32 [R, next_width], written
+ *   workspace    device scratch of workspace_bytes >= gr_beam_select_workspace_size()
+ * Device pointers must be 16-byte aligned (next_parent's rows need not be).
+ * Two kernels on `stream`; nothing is allocated.  Errors: GR_ERR_NULL_ARG,
+ * GR_ERR_BAD_SHAPE, GR_ERR_MISALIGNED, GR_ERR_WORKSPACE_TOO_SMALL,
+ * GR_ERR_UNSUPPORTED, GR_ERR_CUDA.
+ */
+int gr_beam_select(const gr_select_shape *shape, const float *logits, const float *beam_scores,
+                   int32_t *next_parent, int64_t parent_stride, int32_t *next_token,
+                   float *next_score, void *workspace, size_t workspace_bytes,
+                   gr_stream_t stream);
+
+/*
+ * gr_beam_select, plus three CUDA events recorded on `stream`: events[0]
+ * before the per-row kernel, events[1] between it and the per-request merge
+ * kernel, events[2] after the merge.  `events` is a HOST array of 3 created
+ * events; all other arguments and errors are those of gr_beam_select.
+ */
+int gr_beam_select_timed(const gr_select_shape *shape, const float *logits,
+                         const float *beam_scores, int32_t *next_parent, int64_t parent_stride,
+                         int32_t *next_token, float *next_score, void *workspace,
+                         size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events);
+
 /* Static description of a gr_status code. */
 const char *gr_status_string(int status);
 

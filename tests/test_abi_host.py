@@ -108,3 +108,38 @@ def test_utilities_reject_bad_args(lib):
     assert lib.gr_resolve_ancestors(ctypes.byref(_shape()), None, w, 2, FAKE, 0) == -1
     assert lib.gr_resolve_ancestors(ctypes.byref(_shape()), FAKE, w, 7, FAKE, 0) == -2
     assert lib.gr_validate_beam_path(ctypes.byref(_shape()), FAKE, w, 2, None, FAKE, 0) == -1
+
+
+def _sel(**kw):
+    d = dict(num_requests=2, width=4, vocab=100, next_width=8)
+    d.update(kw)
+    return gr.SelectShape(d["num_requests"], d["width"], d["vocab"], d["next_width"])
+
+
+def test_beam_select_workspace_size(lib):
+    # one sorted list of min(next_width, V) 8-byte entries per beam row
+    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel())) == 2 * 4 * 8 * 8
+    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel(vocab=3, next_width=10))) == 2 * 4 * 3 * 8
+    for bad in (dict(num_requests=0), dict(width=0), dict(vocab=0), dict(next_width=0),
+                dict(next_width=1025, vocab=1000), dict(width=2, vocab=3, next_width=7),
+                dict(width=1 << 16, vocab=1 << 15)):
+        assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel(**bad))) == 0, bad
+    assert lib.gr_beam_select_workspace_size(None) == 0
+
+
+def test_beam_select_rejects_bad_args(lib):
+    ok = ctypes.byref(_sel())
+
+    def call(shape=ok, logits=FAKE, scores=FAKE, parent=FAKE, stride=8, token=FAKE, score=FAKE,
+             ws=FAKE, ws_bytes=1 << 20):
+        return lib.gr_beam_select(shape, logits, scores, parent, stride, token, score, ws, ws_bytes, None)
+
+    assert call(shape=None) == -1
+    assert call(logits=None) == -1
+    assert call(parent=None) == -1
+    assert call(ws=None) == -1
+    assert call(shape=ctypes.byref(_sel(next_width=0))) == -2
+    assert call(stride=7) == -2
+    assert call(logits=FAKE + 4) == -4
+    assert call(token=FAKE + 8) == -4
+    assert call(ws_bytes=2 * 4 * 8 * 8 - 1) == -5

@@ -192,3 +192,27 @@ def make_custom(R: int, Hq: int, Hkv: int, D: int, ctx_len: Sequence[int],
         beam_k=beam_k, beam_v=beam_v, beam_path=beam_path,
         widths=np.asarray(W, dtype=np.int32),
     )
+
+
+# --------------------------------------------------------------------------- beam selection
+#
+# Inputs of the beam-selection step that follows a decode forward: next-token
+# logits of every active beam and the beams' cumulative log-probabilities.
+# Recipe: Generator(PCG64(seed)); logits are float32 draws of N(0, sigma^2)
+# (sigma = logit_std), then beam scores -|N(0, 1)| * 3 (cumulative
+# log-probabilities are negative).  The vocabulary defaults to 151,936
+# entries, the Qwen3 tokenizer's embedding rows; the pages measure a fixed
+# width of 900 with full-vocabulary log-probabilities.
+
+SELECT_HEADLINE = dict(num_requests=4, width=900, vocab=151936, next_width=900)
+
+
+def make_select_inputs(num_requests: int, width: int, vocab: int, seed: int,
+                       logit_std: float = 2.0) -> Dict[str, np.ndarray]:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    logits = rng.standard_normal(size=(num_requests, width, vocab), dtype=np.float32)
+    if logit_std != 1.0:
+        logits *= np.float32(logit_std)
+    scores = (-np.abs(rng.standard_normal(size=(num_requests, width), dtype=np.float32))
+              * np.float32(3.0))
+    return dict(logits=logits, beam_scores=scores)
