@@ -382,7 +382,8 @@ int gr_validate_beam_path(const gr_attn_shape *shape, const int32_t *beam_path, 
 
 size_t gr_beam_select_workspace_size(const gr_select_shape *shape) {
     if (!shape || shape->num_requests < 1 || shape->width < 1 || shape->vocab < 1 || shape->next_width < 1 ||
-        shape->next_width > select_max_width() || (long long)shape->width * shape->vocab >= (1LL << 31) ||
+        shape->next_width > select_max_width() || shape->width > select_max_beams() ||
+        (long long)shape->width * shape->vocab >= (1LL << 31) ||
         shape->next_width > (long long)shape->width * shape->vocab)
         return 0;
     return select_list_bytes(shape->num_requests, shape->width, shape->vocab, shape->next_width);

@@ -82,6 +82,7 @@ cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 // gr_select.cu  (beam selection)
 size_t select_list_bytes(int R, int W, int V, int next_width);
 int select_max_width();
+int select_max_beams();
 // `between` (may be null) is recorded on `s` between the two kernels
 cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float *logits,
                                const float *beam_scores, int32_t *next_parent, long long parent_stride,

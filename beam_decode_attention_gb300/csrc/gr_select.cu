@@ -19,16 +19,20 @@
 //                 bounds the candidates the row can contribute;
 //   pass 1 (L2)   every logit at or above that bin (less a margin of a few
 //                 ulps, so that candidates whose rounded scores tie with the
-//                 bin's are kept) is scored and collected in shared memory,
-//                 sorted by (score desc, v asc), and the row's best L go to
-//                 the workspace.
+//                 bin's are kept) is scored and collected in shared memory;
+//                 the row's L-th score is found among them, and those that
+//                 can still be selected are sorted by (score desc, v asc)
+//                 and written to the workspace.
 //   A row whose boundary bin holds more than the shared-memory capacity
 //   (ties, peaked or degenerate logits) takes an exact radix select on the
 //   scores instead (more passes, same result).
+// Each row also publishes its L-th score key (atomicMax per request): with
+// L = W' that row alone holds W' candidates at or above it, so it bounds the
+// request's W'-th score from below.
 // Kernel 2 (select_merge_kernel), one CTA per request: the W'-th largest
-// score over the sorted row lists by bisection on the ordered key, the
-// candidates above it plus the tied ones in flat-index order, and a final
-// sort by (score desc, flat index asc).
+// score over the row lists' prefixes at or above that bound, by a radix
+// select in shared memory; the candidates above it plus the tied ones in
+// flat-index order; and a final sort by (score desc, flat index asc).
 #include <cstdint>
 #include <mutex>
 
@@ -46,6 +50,15 @@ constexpr int kCap = 4096;            // candidate slots per row in shared memor
 constexpr int kMergeThreads = 1024;
 constexpr int kMaxSel = 1024;         // GR_SELECT_MAX_WIDTH
 
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+
+// 2^x on the MUFU unit (ex2.approx)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Order-preserving map of an fp32 value to uint32 (-0 taken as +0).
 __device__ __forceinline__ uint32_t ord_key(float x) {
     if (x == 0.f) x = 0.f;
@@ -60,7 +73,9 @@ struct RowArgs {
     const float *logits;
     const float *beam_scores;
     unsigned long long *lists;   // [R * W_s][L] (score key << 32 | ~v), sorted descending
-    int rows, V, L;
+    int *plen;                   // [R * W_s] entries written to each list (<= L)
+    unsigned *tau_lb;            // [R] lower bound on each request's W'-th score key (null: none)
+    int rows, W, V, L;
 };
 
 // The fp32 score of logit z in a row with log-normaliser c and beam score S:
@@ -120,19 +135,6 @@ __device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
     if (a.m == -INFINITY) return b;
     const float m = fmaxf(a.m, b.m);
     return {m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
-}
-
-// Block-wide sum (all threads get it); `red` holds one int per warp.
-__device__ __forceinline__ int block_sum(int x, int *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFullMask, x, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    int t = 0;
-    for (int w = 0; w < nw; ++w) t += red[w];
-    return t;
 }
 
 // Exclusive prefix sum over the block in thread order (all threads take part);
@@ -204,6 +206,25 @@ __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t low) {
     return ((unsigned long long)key << 32) | low;
 }
 
+// Keeps the entries e of a[0, n) with keep(e), transformed by xf(e), at the
+// front of a, in their order (chunk by chunk, a block-wide scan each);
+// returns the count (every thread).
+template <typename Keep, typename Xf>
+__device__ __forceinline__ int compact(unsigned long long *arr, int n, int *red, Keep &&keep, Xf &&xf) {
+    int kept = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        const unsigned long long e = i < n ? arr[i] : 0ull;
+        const int f = (i < n && keep(e)) ? 1 : 0;
+        int tot;
+        const int pos = block_excl_scan(f, red, &tot);   // synchronises before any write below
+        if (f) arr[kept + pos] = xf(e);
+        kept += tot;
+        __syncthreads();
+    }
+    return kept;
+}
+
 __global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) {
     extern __shared__ unsigned long long sel_smem[];
     unsigned long long *cand = sel_smem;                          // [kCap]
@@ -219,12 +240,75 @@ __global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) 
         for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
         __syncthreads();
 
-        // pass 0: maximum, sum of exponentials, histogram of the logits' keys
+        // pass 0: maximum and sum of exponentials of every logit, and a
+        // histogram of the logits' keys.  Once L logits are counted, the bin
+        // holding the L-th largest of them is a lower bound on the row's
+        // boundary bin (the L-th largest of a subset is not above the row's),
+        // so later logits below it are not counted: the counts from that bin
+        // up stay exact, and most logits skip the shared-memory atomics.
         MaxSum ms{-INFINITY, 0.f};
-        for_row(z, a.V, [&](float x, int) {
-            ms = ms_add(ms, x);
-            atomicAdd(&hist[ord_key(x) >> (32 - kHistBits)], 1);
-        });
+        {
+            int lb = 0;
+            float zg = -INFINITY;   // the smallest logit of bin lb: x >= zg <=> bin(x) >= lb
+            auto visit = [&](float x) {   // head and tail logits, before any bound
+                ms = ms_add(ms, x);
+                atomicAdd(&hist[ord_key(x) >> (32 - kHistBits)], 1);
+            };
+            const int head = min(a.V, (int)(((16 - (reinterpret_cast<uintptr_t>(z) & 15)) & 15) >> 2));
+            const int n4 = (a.V - head) >> 2, tail = head + 4 * n4;
+            for (int v = threadIdx.x; v < head; v += blockDim.x) visit(__ldg(z + v));
+            for (int v = tail + threadIdx.x; v < a.V; v += blockDim.x) visit(__ldg(z + v));
+            const float4 *row4 = reinterpret_cast<const float4 *>(z + head);
+            constexpr int kU = 8;   // 8 x 16 B in flight per thread
+            const int chunk4 = kU * blockDim.x;
+            long long seen = head + (a.V - tail);
+            for (int c0 = 0, ci = 0; c0 < n4; c0 += chunk4, ++ci) {
+                float4 x[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = c0 + threadIdx.x + u * blockDim.x;
+                    if (i < n4) x[u] = __ldg(row4 + i);
+                }
+                // the chunk's maximum first, then its exponentials (independent
+                // of each other), merged into the running pair once per chunk
+                float cm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = c0 + threadIdx.x + u * blockDim.x;
+                    if (i >= n4) x[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+                }
+                if (cm != -INFINITY) {
+                    // e^(x - cm) = 2^(x log2e - cm log2e): one FMA and one ex2 each
+                    const float off = -cm * kLog2e;
+                    float cs = 0.f;
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        cs += (ex2_approx(fmaf(x[u].x, kLog2e, off)) + ex2_approx(fmaf(x[u].y, kLog2e, off))) +
+                              (ex2_approx(fmaf(x[u].z, kLog2e, off)) + ex2_approx(fmaf(x[u].w, kLog2e, off)));
+                    ms = ms_merge(ms, MaxSum{cm, cs});
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = c0 + threadIdx.x + u * blockDim.x;
+                    if (i < n4) {
+                        const float q[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (q[e] >= zg) atomicAdd(&hist[ord_key(q[e]) >> (32 - kHistBits)], 1);
+                    }
+                }
+                seen += 4LL * min(chunk4, n4 - c0);
+                // tighten the bound after chunks 0, 1, 3 and 7
+                if (seen >= a.L && c0 + chunk4 < n4 && (ci & (ci + 1)) == 0 && ci < 8) {
+                    __syncthreads();
+                    find_bin(hist, a.L, red, &s_bin, &s_above);
+                    lb = s_bin;
+                    // bins at or below 7 hold -inf and NaN patterns: no bound there
+                    zg = lb <= 7 ? -INFINITY : key_float((uint32_t)lb << (32 - kHistBits));
+                }
+            }
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
@@ -319,19 +403,73 @@ __global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) 
             __syncthreads();
             n = min(s_cnt, kCap);
         }
+        // The row's L-th largest score key among the n candidates (radix
+        // select in shared memory).  With L = W' this row alone holds W'
+        // candidates at or above it, so it bounds the request's W'-th score
+        // from below: it is published, and no candidate under the larger of
+        // it and the bound published so far can be selected, so only those
+        // at or above are kept (the row's best, at most L of them).
+        uint32_t kl = 0u;
+        {
+            uint32_t prefix = 0, mask = 0;
+            int need = a.L;
+            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+            for (int rd = 0; rd < 3; ++rd) {
+                for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+                __syncthreads();
+                const int sh = shifts[rd];
+                const uint32_t bm = (1u << widths[rd]) - 1u;
+                for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                    const uint32_t k = (uint32_t)(cand[i] >> 32);
+                    if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
+                }
+                __syncthreads();
+                find_bin(hist, need, red, &s_bin, &s_above);
+                need -= s_above;
+                prefix |= (bm - (uint32_t)(kHistBins - 1 - s_bin)) << sh;
+                mask |= bm << sh;
+                __syncthreads();
+            }
+            kl = prefix;
+        }
+        uint32_t keep = kl;
+        if (a.tau_lb) {
+            const uint32_t lbnow = *reinterpret_cast<volatile unsigned *>(a.tau_lb + row / a.W);
+            keep = lbnow > keep ? lbnow : keep;
+        }
+        // compact the candidates with key >= keep to the front, chunk by chunk
+        int kept = 0;
+        for (int base = 0; base < n; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            const unsigned long long e = i < n ? cand[i] : 0ull;
+            const int f = (i < n && (uint32_t)(e >> 32) >= keep) ? 1 : 0;
+            int tot;
+            const int pos = block_excl_scan(f, red, &tot);   // synchronises before any write below
+            if (f) cand[kept + pos] = e;
+            kept += tot;
+            __syncthreads();
+        }
         int np2 = 1;
-        while (np2 < n) np2 <<= 1;
-        for (int i = n + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
+        while (np2 < kept) np2 <<= 1;
+        for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
         __syncthreads();
         bitonic_desc(cand, np2);
+        const int cnt = min(kept, a.L);
         unsigned long long *out = a.lists + (long long)row * a.L;
-        for (int j = threadIdx.x; j < a.L; j += blockDim.x) out[j] = cand[j];
+        for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = cand[j];
+        if (threadIdx.x == 0) {
+            a.plen[row] = cnt;
+            if (a.tau_lb) atomicMax(a.tau_lb + row / a.W, kl);
+        }
         __syncthreads();
     }
 }
 
 struct MergeSelArgs {
     const unsigned long long *lists;
+    const unsigned *tau_lb;
+    const int *plen;   // [R * W_s] entries of each row list
     int W, V, L, next_width;
     int32_t *next_parent;
     long long parent_stride;
@@ -339,67 +477,187 @@ struct MergeSelArgs {
     float *next_score;
 };
 
-// number of entries of a descending list (key in the high 32 bits) with key >= t
-__device__ __forceinline__ int count_ge(const unsigned long long *lst, int L, uint32_t t) {
-    int lo = 0, hi = L;   // first index whose key < t
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((uint32_t)(lst[mid] >> 32) >= t) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
+// dynamic shared memory of the merge kernel: list offsets, per-list counts
+// above and tied with the threshold, the histogram and the selection
+constexpr int kMaxBeams = 4096;   // GR_SELECT_MAX_BEAMS
+constexpr int kMergeSmem = (3 * (kMaxBeams + 1) + kHistBins) * 4 + kMaxSel * 8;
 
+// One CTA per request.  Each row list holds the row's best candidates down to
+// the bound that row saw; only entries at or above the final lower bound can
+// be selected.  The entries of all lists are walked as one flat range (list
+// offsets in shared memory), so every thread keeps several independent loads
+// in flight.  The W'-th largest key is found by a radix select (12 + 12 + 8
+// bits), then every key above it is taken and the tied ones in flat-index
+// order (lists in b order, each list in v order: the lists are sorted), and
+// the W' are sorted by (score desc, flat asc).
 __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSelArgs a) {
-    __shared__ unsigned long long sel[kMaxSel];
+    extern __shared__ unsigned long long msm[];
+    unsigned long long *sel = msm;                           // [kMaxSel] (8-byte entries first)
+    int *offs = reinterpret_cast<int *>(sel + kMaxSel);      // [W + 1]
+    int *gtc = offs + (kMaxBeams + 1);                       // [W + 1] entries above tau, then offsets
+    int *eqc = gtc + (kMaxBeams + 1);                        // [W + 1] entries tied with tau, then offsets
+    int *hist = eqc + (kMaxBeams + 1);                       // [kHistBins]
     __shared__ int red[32];
+    __shared__ int s_bin, s_above;
     const int r = blockIdx.x;
     const unsigned long long *lists = a.lists + (long long)r * a.W * a.L;
-    // lists b in [b0, b1) belong to this thread (consecutive, for in-order prefixes)
+    const int *plen = a.plen + (long long)r * a.W;
+    uint32_t lb = a.tau_lb ? a.tau_lb[r] : 0u;
     const int per = (a.W + blockDim.x - 1) / blockDim.x;
     const int b0 = min(a.W, (int)threadIdx.x * per), b1 = min(a.W, b0 + per);
-    auto count_all = [&](uint32_t t) {
-        int c = 0;
-        for (int b = b0; b < b1; ++b) c += count_ge(lists + (long long)b * a.L, a.L, t);
-        return block_sum(c, red);
-    };
-    // tau = the largest key t with at least next_width entries >= t
-    uint32_t lo = 0u, hi = 0xffffffffu;
-    while (lo < hi) {
-        const uint32_t mid = lo + (uint32_t)(((unsigned long long)hi - lo + 1ull) >> 1);
-        if (count_all(mid) >= a.next_width) lo = mid;
-        else hi = mid - 1u;
+    // A tighter bound: the next_width-th largest key among the first kh keys
+    // of every list (real candidates, so at least next_width entries reach it).
+    {
+        const int kh = min(32, max(1, (4 * a.next_width + a.W - 1) / a.W));
+        // the keys go where offs, gtc and eqc will be (not yet in use)
+        unsigned *heads = reinterpret_cast<unsigned *>(offs);
+        const int cap = 3 * (kMaxBeams + 1);
+        int nh = 0;
+        if (a.W * kh <= cap) {
+            for (int t = threadIdx.x; t < a.W * kh; t += blockDim.x) {
+                const int b = t / kh, j = t % kh;
+                heads[t] = j < plen[b] ? (unsigned)(lists[(long long)b * a.L + j] >> 32) : 0u;
+            }
+            nh = a.W * kh;
+        }
+        __syncthreads();
+        if (nh >= a.next_width) {
+            uint32_t prefix = 0, mask = 0;
+            int need = a.next_width;
+            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+            for (int rd = 0; rd < 3; ++rd) {
+                for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+                __syncthreads();
+                const int sh = shifts[rd];
+                const uint32_t bm = (1u << widths[rd]) - 1u;
+                for (int i = threadIdx.x; i < nh; i += blockDim.x) {
+                    const uint32_t k = heads[i];
+                    if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
+                }
+                __syncthreads();
+                find_bin(hist, need, red, &s_bin, &s_above);
+                need -= s_above;
+                prefix |= (bm - (uint32_t)(kHistBins - 1 - s_bin)) << sh;
+                mask |= bm << sh;
+                __syncthreads();
+            }
+            lb = prefix > lb ? prefix : lb;
+        }
     }
-    const uint32_t tau = lo;
-    // per list: entries above tau (all taken) and tied with tau (taken in
-    // flat-index order: lists in b order, each list in v order)
-    int gt = 0, eq = 0;
+    // per list, the sorted prefix at or above the bound (binary search), then
+    // the list offsets: lists [b0, b1) of this thread are consecutive
+    int mine = 0;
     for (int b = b0; b < b1; ++b) {
         const unsigned long long *lst = lists + (long long)b * a.L;
-        const int ge = count_ge(lst, a.L, tau);
-        const int g = tau == 0xffffffffu ? 0 : count_ge(lst, a.L, tau + 1u);
-        gt += g;
-        eq += ge - g;
+        int lo = 0, hi = plen[b];   // first index whose key < lb
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((uint32_t)(lst[mid] >> 32) >= lb) lo = mid + 1;
+            else hi = mid;
+        }
+        gtc[b] = lo;   // the prefix length, for now
+        mine += lo;
+    }
+    int total;
+    int off = block_excl_scan(mine, red, &total);
+    for (int b = b0; b < b1; ++b) {
+        offs[b] = off;
+        off += gtc[b];
+        gtc[b] = 0;
+        eqc[b] = 0;
+    }
+    if (threadIdx.x == 0) offs[a.W] = total;
+    __syncthreads();
+    // entry e of the flat range: list b (offs[b] <= e < offs[b+1]) and index j
+    auto locate = [&](int e, int &b, int &j) {
+        int lo = 0, hi = a.W;   // the last b with offs[b] <= e
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offs[mid] <= e) lo = mid;
+            else hi = mid;
+        }
+        b = lo;
+        j = e - offs[lo];
+    };
+    constexpr int kIn = 4;   // loads in flight per thread
+    // radix select of the next_width-th largest key
+    uint32_t prefix = 0, mask = 0;
+    int need = a.next_width;
+    const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+    for (int rd = 0; rd < 3; ++rd) {
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        const int sh = shifts[rd];
+        const uint32_t bm = (1u << widths[rd]) - 1u;
+        for (int e0 = threadIdx.x; e0 < total; e0 += kIn * blockDim.x) {
+            uint32_t k[kIn];
+#pragma unroll
+            for (int u = 0; u < kIn; ++u) {
+                const int e = e0 + u * blockDim.x;
+                k[u] = 0u;
+                if (e < total) {
+                    int b, j;
+                    locate(e, b, j);
+                    k[u] = (uint32_t)(lists[(long long)b * a.L + j] >> 32);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kIn; ++u)
+                if (e0 + u * blockDim.x < total && k[u] >= lb && (k[u] & mask) == prefix)
+                    atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k[u] >> sh) & bm))], 1);
+        }
+        __syncthreads();
+        find_bin(hist, need, red, &s_bin, &s_above);
+        need -= s_above;
+        prefix |= (bm - (uint32_t)(kHistBins - 1 - s_bin)) << sh;
+        mask |= bm << sh;
+        __syncthreads();
+    }
+    const uint32_t tau = prefix;   // need = how many entries equal to tau are taken
+    // per list: entries above tau and tied with it (runs at the list's front)
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        int b, j;
+        locate(e, b, j);
+        const uint32_t k = (uint32_t)(lists[(long long)b * a.L + j] >> 32);
+        if (k > tau) atomicAdd(&gtc[b], 1);
+        else if (k == tau) atomicAdd(&eqc[b], 1);
+    }
+    __syncthreads();
+    int gt = 0, eq = 0;
+    for (int b = b0; b < b1; ++b) {
+        gt += gtc[b];
+        eq += eqc[b];
     }
     int n_gt, n_eq;
     int pos_gt = block_excl_scan(gt, red, &n_gt);
     int pos_eq = block_excl_scan(eq, red, &n_eq);
-    const int need = a.next_width - n_gt;
+    // the counts become offsets (in b order); entry W holds the totals, so a
+    // list's count is the next offset minus its own
     for (int b = b0; b < b1; ++b) {
-        const unsigned long long *lst = lists + (long long)b * a.L;
-        const int ge = count_ge(lst, a.L, tau);
-        const int g = tau == 0xffffffffu ? 0 : count_ge(lst, a.L, tau + 1u);
-        for (int j = 0; j < ge; ++j) {
-            const unsigned long long e = lst[j];
-            const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)e;
-            const unsigned long long item = ((e >> 32) << 32) | (uint32_t)~flat;
-            if (j < g) {
-                sel[pos_gt++] = item;
-            } else if (pos_eq < need) {
-                sel[n_gt + pos_eq] = item;
-                ++pos_eq;
-            }
-        }
+        const int g = gtc[b], q = eqc[b];
+        gtc[b] = pos_gt;
+        eqc[b] = pos_eq;
+        pos_gt += g;
+        pos_eq += q;
+    }
+    if (threadIdx.x == 0) {
+        gtc[a.W] = n_gt;
+        eqc[a.W] = n_eq;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        int b, j;
+        locate(e, b, j);
+        const int og = gtc[b], g = gtc[b + 1] - og;
+        const int oe = eqc[b], q = eqc[b + 1] - oe;
+        if (j >= g + q) continue;
+        const unsigned long long ent = lists[(long long)b * a.L + j];
+        const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)ent;
+        const unsigned long long item = ((ent >> 32) << 32) | (uint32_t)~flat;
+        if (j < g) sel[og + j] = item;
+        else if (oe + (j - g) < need) sel[n_gt + oe + (j - g)] = item;
     }
     __syncthreads();
     int np2 = 1;
@@ -418,12 +676,18 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
 
 }  // namespace
 
+// workspace: row lists [R * W][L] u64 | lower bounds [R] u32 (16-byte padded) |
+// list lengths [R * W] int32
+static size_t list_bytes(int R, int W, int L) { return (size_t)R * W * L * sizeof(unsigned long long); }
+static size_t bound_bytes(int R) { return ((size_t)R * 4 + 15) / 16 * 16; }
+
 size_t select_list_bytes(int R, int W, int V, int next_width) {
-    const long long L = next_width < V ? next_width : V;
-    return (size_t)R * W * L * sizeof(unsigned long long);
+    const int L = next_width < V ? next_width : V;
+    return list_bytes(R, W, L) + bound_bytes(R) + (size_t)R * W * sizeof(int);
 }
 
 int select_max_width() { return kMaxSel; }
+int select_max_beams() { return kMaxBeams; }
 
 cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float *logits,
                                const float *beam_scores, int32_t *next_parent, long long parent_stride,
@@ -443,17 +707,33 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kCap * 8 + kHistBins * 4 + 32 * 4);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(select_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMergeSmem);
             if (e != cudaSuccess) return e;
             sm_count[dev] = n;
         }
     }
+    const int L = next_width < V ? next_width : V;
+    unsigned char *wsb = static_cast<unsigned char *>(workspace);
+    unsigned *tau_lb = reinterpret_cast<unsigned *>(wsb + list_bytes(R, W, L));
+    int *counts = reinterpret_cast<int *>(wsb + list_bytes(R, W, L) + bound_bytes(R));
+    // the bound is only valid when a row alone holds W' candidates (V >= W')
+    const bool bound = L == next_width;
+    if (bound) {
+        e = cudaMemsetAsync(tau_lb, 0, (size_t)R * 4, s);
+        if (e != cudaSuccess) return e;
+    }
     RowArgs ra;
     ra.logits = logits;
     ra.beam_scores = beam_scores;
-    ra.lists = static_cast<unsigned long long *>(workspace);
+    ra.lists = reinterpret_cast<unsigned long long *>(wsb);
+    ra.tau_lb = bound ? tau_lb : nullptr;
+    ra.plen = counts;
     ra.rows = R * W;
+    ra.W = W;
     ra.V = V;
-    ra.L = next_width < V ? next_width : V;
+    ra.L = L;
     const int smem = kCap * 8 + kHistBins * 4 + 32 * 4;
     const int grid = ra.rows < sm_count[dev] ? ra.rows : sm_count[dev];
     select_rows_kernel<<<grid, kRowThreads, smem, s>>>(ra);
@@ -462,6 +742,8 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     if (e != cudaSuccess) return e;
     MergeSelArgs ma;
     ma.lists = ra.lists;
+    ma.tau_lb = ra.tau_lb;
+    ma.plen = counts;
     ma.W = W;
     ma.V = V;
     ma.L = ra.L;
@@ -470,7 +752,7 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ma.parent_stride = parent_stride;
     ma.next_token = next_token;
     ma.next_score = next_score;
-    select_merge_kernel<<<R, kMergeThreads, 0, s>>>(ma);
+    select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
     return cudaGetLastError();
 }
 

@@ -104,15 +104,18 @@ def peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_hash():
+SELECT_KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_select.cu"]
+
+
+def kernel_hash(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, sources=None):
     """DRAM bytes per launch of the dominant kernel from a committed ncu
     summary, only while the kernel source is unchanged since it was taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -121,7 +124,7 @@ def recorded_traffic(workload):
     with open(path) as fh:
         d = json.load(fh)
     ent = d.get(workload)
-    if not ent or ent.get("kernel_sha") != kernel_hash():
+    if not ent or ent.get("kernel_sha") != kernel_hash(sources):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -354,7 +357,8 @@ def run_select_bench(args):
                    "l2": "inputs (2.19 GB of logits per call) larger than L2; no flush"},
         "row_kernel_us": float(np.mean(rows_us)), "merge_kernel_us": float(np.mean(call_us) - np.mean(rows_us)),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 3), "traffic": None,
+                     "frac": round(achieved / pk["hbm_gbs"], 3),
+                     "traffic": recorded_traffic("beam_select_r4_w900_v151936", SELECT_KERNEL_SOURCES),
                      "kernel": "select_rows_kernel", "peak_source": pk.get("source", "measured copy")},
         "gpu_launches": 2 * args.steps, "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
     }

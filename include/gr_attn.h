@@ -237,10 +237,11 @@ int gr_get_device_error(void);
  * finite logit, and no logit may be NaN or +inf (not checked).
  */
 #define GR_SELECT_MAX_WIDTH 1024
+#define GR_SELECT_MAX_BEAMS 4096
 
 typedef struct {
     int32_t num_requests; /* R >= 1 */
-    int32_t width;        /* W_s >= 1: active beams per request */
+    int32_t width;        /* W_s: 1 <= W_s <= GR_SELECT_MAX_BEAMS active beams per request */
     int32_t vocab;        /* V >= 1: logits per beam; W_s * V < 2^31 */
     int32_t next_width;   /* W': 1 <= W' <= min(GR_SELECT_MAX_WIDTH, W_s * V) */
 } gr_select_shape;

@@ -116,13 +116,18 @@ def _sel(**kw):
     return gr.SelectShape(d["num_requests"], d["width"], d["vocab"], d["next_width"])
 
 
+def _sel_bytes(R, W, V, n):
+    # per beam row a sorted list of min(n, V) 8-byte entries and its length;
+    # per request a 4-byte bound (padded to 16 bytes)
+    return R * W * min(n, V) * 8 + (R * 4 + 15) // 16 * 16 + R * W * 4
+
+
 def test_beam_select_workspace_size(lib):
-    # one sorted list of min(next_width, V) 8-byte entries per beam row
-    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel())) == 2 * 4 * 8 * 8
-    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel(vocab=3, next_width=10))) == 2 * 4 * 3 * 8
+    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel())) == _sel_bytes(2, 4, 100, 8)
+    assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel(vocab=3, next_width=10))) == _sel_bytes(2, 4, 3, 10)
     for bad in (dict(num_requests=0), dict(width=0), dict(vocab=0), dict(next_width=0),
                 dict(next_width=1025, vocab=1000), dict(width=2, vocab=3, next_width=7),
-                dict(width=1 << 16, vocab=1 << 15)):
+                dict(width=1 << 16, vocab=1 << 15), dict(width=4097, vocab=10)):
         assert lib.gr_beam_select_workspace_size(ctypes.byref(_sel(**bad))) == 0, bad
     assert lib.gr_beam_select_workspace_size(None) == 0
 
@@ -142,4 +147,4 @@ def test_beam_select_rejects_bad_args(lib):
     assert call(stride=7) == -2
     assert call(logits=FAKE + 4) == -4
     assert call(token=FAKE + 8) == -4
-    assert call(ws_bytes=2 * 4 * 8 * 8 - 1) == -5
+    assert call(ws_bytes=_sel_bytes(2, 4, 100, 8) - 1) == -5
