@@ -83,14 +83,14 @@ struct RowArgs {
 __device__ __forceinline__ float score_of(float z, float c, float S) { return S + (z - c); }
 
 // Visit z = row[v] for v in [0, V): 16-byte loads where the row allows, in
-// groups of four per thread so that several loads are in flight.
+// groups of eight per thread so that several loads are in flight.
 template <typename F>
 __device__ __forceinline__ void for_row(const float *row, int V, F &&f) {
     const int head = min(V, (int)(((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15) >> 2));
     for (int v = threadIdx.x; v < head; v += blockDim.x) f(__ldg(row + v), v);
     const float4 *row4 = reinterpret_cast<const float4 *>(row + head);
     const int n4 = (V - head) >> 2;
-    constexpr int kU = 4;
+    constexpr int kU = 8;
     int i = threadIdx.x;
     for (; i + (kU - 1) * (int)blockDim.x < n4; i += kU * blockDim.x) {
         float4 x[kU];
