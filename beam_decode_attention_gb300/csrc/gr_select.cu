@@ -14,9 +14,10 @@
 // rows with one CTA per SM, so that a row re-read right after its first pass
 // still sits in L2:
 //   pass 0 (HBM)  the row's maximum and sum of exponentials, and a 4096-bin
-//                 histogram of the logits' ordered bit patterns (top 12 bits);
-//                 the bin holding the row's L-th largest logit (L = min(W', V))
-//                 bounds the candidates the row can contribute;
+//                 histogram of the logits' ordered bit patterns (top 12 bits),
+//                 counted only above a lower bound that tightens as the row
+//                 streams; the bin holding the row's L-th largest logit
+//                 (L = min(W', V)) bounds the candidates the row can contribute;
 //   pass 1 (L2)   every logit at or above that bin (less a margin of a few
 //                 ulps, so that candidates whose rounded scores tie with the
 //                 bin's are kept) is scored and collected in shared memory;
@@ -29,10 +30,11 @@
 // Each row also publishes its L-th score key (atomicMax per request): with
 // L = W' that row alone holds W' candidates at or above it, so it bounds the
 // request's W'-th score from below.
-// Kernel 2 (select_merge_kernel), one CTA per request: the W'-th largest
-// score over the row lists' prefixes at or above that bound, by a radix
-// select in shared memory; the candidates above it plus the tied ones in
-// flat-index order; and a final sort by (score desc, flat index asc).
+// Kernel 2 (select_merge_kernel), one CTA per request: a tighter bound from
+// the first keys of every list; each sorted list's prefix at or above it; the
+// W'-th largest score over those prefixes by a radix select in shared
+// memory; the candidates above it plus the tied ones in flat-index order;
+// and a final sort by (score desc, flat index asc).
 #include <cstdint>
 #include <mutex>
 
