@@ -100,3 +100,67 @@ def top_candidates(logits: np.ndarray, beam_scores: np.ndarray, next_width: int,
         flats.append(keep)
         vals.append(sc[keep])
     return np.stack(flats), np.stack(vals)
+
+
+# --------------------------------------------------------------------------- item-constrained selection
+#
+# GR-Inference blog, "kernel design" (the item-constrained fused kernel: the
+# SID trie resident on the device in CSR form; prefix traversal, gather of
+# the legal tokens and a local top-K, with no full-vocabulary mask); xGR
+# review, "xBeam" (an item mask on the logits filters invalid token ids).
+#
+# Trie in CSR form: node n's children are the edges k in
+# [offsets[n], offsets[n+1]), each with a token tokens[k] (strictly
+# increasing within a node) and a child node children[k].  Beam b of request
+# r sits at node beam_node[r, b] (the node its SID prefix reached; the root
+# at the first step).  Its legal next tokens are that node's edge tokens, and
+# masking every other logit to -inf before log_softmax means:
+#
+#     lp[r, b, k] = z[r, b, tokens[k]] - ln sum_{k' legal} exp(z[r, b, tokens[k']])
+#     score       = S[r, b] + lp
+#
+# The next W' beams are the W' largest scores over every beam's legal
+# candidates, equal scores ordered by the smaller flat index b * V + token;
+# each keeps its parent b, its token, its score and its child node (the
+# traversal advances one level per step).  A beam at a leaf has no
+# candidates; when a request has fewer than W' candidates the remaining
+# slots hold parent -1, token -1, score -inf and node -1.
+
+
+def trie_select(logits: np.ndarray, beam_scores: np.ndarray, beam_node: np.ndarray,
+                offsets: np.ndarray, tokens: np.ndarray, children: np.ndarray,
+                next_width: int):
+    """Returns parent, token, node (int32 [R, W']) and score (fp64 [R, W'])."""
+    z = np.asarray(logits, dtype=np.float64)
+    S = np.asarray(beam_scores, dtype=np.float64)
+    R, W, V = z.shape
+    parent = np.full((R, next_width), -1, np.int32)
+    token = np.full((R, next_width), -1, np.int32)
+    node = np.full((R, next_width), -1, np.int32)
+    best = np.full((R, next_width), -np.inf)
+    for r in range(R):
+        flats, vals, kids = [], [], []
+        for b in range(W):
+            n = int(beam_node[r, b])
+            ks = np.arange(int(offsets[n]), int(offsets[n + 1]))
+            if ks.size == 0:
+                continue
+            toks = np.asarray(tokens)[ks]
+            lz = z[r, b, toks]
+            m = lz.max()
+            lp = lz - (m + np.log(np.sum(np.exp(lz - m))))
+            flats.append(b * V + toks.astype(np.int64))
+            vals.append(S[r, b] + lp)
+            kids.append(np.asarray(children)[ks])
+        if not flats:
+            continue
+        flat = np.concatenate(flats)
+        val = np.concatenate(vals)
+        kid = np.concatenate(kids)
+        order = np.lexsort((flat, -val))[:next_width]
+        n_take = order.size
+        parent[r, :n_take] = flat[order] // V
+        token[r, :n_take] = flat[order] % V
+        node[r, :n_take] = kid[order]
+        best[r, :n_take] = val[order]
+    return parent, token, node, best
