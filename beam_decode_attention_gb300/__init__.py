@@ -32,6 +32,7 @@ __all__ = [
     "gr_version", "EXPORTED_SYMBOLS", "gr_decode_attn_timed", "gr_decode_attn_plan", "PlanInfo",
     "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES", "SelectShape", "gr_beam_select",
     "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
+    "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -39,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
     "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
+    "gr_trie_select_workspace_size", "gr_trie_select",
 )
 
 # GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
@@ -88,6 +90,18 @@ class SelectShape(ctypes.Structure):
         ("width", ctypes.c_int32),
         ("vocab", ctypes.c_int32),
         ("next_width", ctypes.c_int32),
+    ]
+
+
+class TrieSelectShape(ctypes.Structure):
+    """``gr_trie_select_shape``."""
+    _fields_ = [
+        ("num_requests", ctypes.c_int32),
+        ("width", ctypes.c_int32),
+        ("vocab", ctypes.c_int32),
+        ("next_width", ctypes.c_int32),
+        ("num_nodes", ctypes.c_int32),
+        ("num_edges", ctypes.c_int32),
     ]
 
 
@@ -147,6 +161,11 @@ def load() -> ctypes.CDLL:
     lib.gr_beam_select.restype = ctypes.c_int
     lib.gr_beam_select_timed.argtypes = [ssp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, sz, vp, vp]
     lib.gr_beam_select_timed.restype = ctypes.c_int
+    tsp = ctypes.POINTER(TrieSelectShape)
+    lib.gr_trie_select_workspace_size.argtypes = [tsp]
+    lib.gr_trie_select_workspace_size.restype = sz
+    lib.gr_trie_select.argtypes = [tsp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz, vp]
+    lib.gr_trie_select.restype = ctypes.c_int
     lib.gr_get_device_error.argtypes = []
     lib.gr_get_device_error.restype = ctypes.c_int
     lib.gr_status_string.argtypes = [ctypes.c_int]
@@ -314,6 +333,27 @@ def gr_beam_select_timed(shape: SelectShape, logits, beam_scores, next_parent, n
                                      _ptr(next_score), _ptr(workspace), int(workspace_bytes),
                                      _stream_handle(stream), ev)
     _check(rc, "gr_beam_select_timed")
+
+
+def gr_trie_select_workspace_size(shape: TrieSelectShape) -> int:
+    return int(load().gr_trie_select_workspace_size(ctypes.byref(shape)))
+
+
+def gr_trie_select(shape: TrieSelectShape, logits, beam_scores, beam_node, trie_offsets, trie_tokens,
+                   trie_children, next_parent, next_token, next_score, next_node, workspace,
+                   parent_stride: Optional[int] = None, workspace_bytes: Optional[int] = None,
+                   stream=None) -> None:
+    """Enqueue gr_trie_select (item-constrained beam selection) on ``stream``."""
+    if parent_stride is None:
+        parent_stride = shape.next_width
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().gr_trie_select(ctypes.byref(shape), _ptr(logits), _ptr(beam_scores), _ptr(beam_node),
+                               _ptr(trie_offsets), _ptr(trie_tokens), _ptr(trie_children),
+                               _ptr(next_parent), int(parent_stride), _ptr(next_token),
+                               _ptr(next_score), _ptr(next_node), _ptr(workspace), int(workspace_bytes),
+                               _stream_handle(stream))
+    _check(rc, "gr_trie_select")
 
 
 def gr_get_device_error() -> int:

@@ -432,6 +432,41 @@ int gr_beam_select_timed(const gr_select_shape *shape, const float *logits, cons
                             workspace, workspace_bytes, stream, events);
 }
 
+size_t gr_trie_select_workspace_size(const gr_trie_select_shape *shape) {
+    if (!shape || shape->num_requests < 1 || shape->width < 1 || shape->vocab < 1 || shape->next_width < 1 ||
+        shape->next_width > select_max_width() || shape->width > select_max_beams() || shape->num_nodes < 1 ||
+        shape->num_edges < 0 || (long long)shape->width * shape->vocab >= (1LL << 31))
+        return 0;
+    return trie_select_bytes(shape->num_requests, shape->width, shape->next_width);
+}
+
+int gr_trie_select(const gr_trie_select_shape *shape, const float *logits, const float *beam_scores,
+                   const int32_t *beam_node, const int32_t *trie_offsets, const int32_t *trie_tokens,
+                   const int32_t *trie_children, int32_t *next_parent, int64_t parent_stride, int32_t *next_token,
+                   float *next_score, int32_t *next_node, void *workspace, size_t workspace_bytes,
+                   gr_stream_t stream) {
+    if (!shape || !logits || !beam_scores || !beam_node || !trie_offsets || !next_parent || !next_token ||
+        !next_score || !next_node || !workspace)
+        return GR_ERR_NULL_ARG;
+    if (shape->num_edges > 0 && (!trie_tokens || !trie_children)) return GR_ERR_NULL_ARG;
+    const size_t need = gr_trie_select_workspace_size(shape);
+    if (need == 0 || parent_stride < shape->next_width) return GR_ERR_BAD_SHAPE;
+    if (misaligned(logits) || misaligned(beam_scores) || misaligned(beam_node) || misaligned(trie_offsets) ||
+        (trie_tokens && misaligned(trie_tokens)) || (trie_children && misaligned(trie_children)) ||
+        misaligned(next_parent) || misaligned(next_token) || misaligned(next_score) || misaligned(next_node) ||
+        misaligned(workspace))
+        return GR_ERR_MISALIGNED;
+    if (workspace_bytes < need) return GR_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo dev;
+    const int rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_trie_select(shape->num_requests, shape->width, shape->vocab, shape->next_width,
+                                          shape->num_nodes, shape->num_edges, logits, beam_scores, beam_node,
+                                          trie_offsets, trie_tokens, trie_children, next_parent,
+                                          (long long)parent_stride, next_token, next_score, next_node, workspace,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 int gr_get_device_error(void) {
     DeviceInfo dev;
     int rc = device_info(&dev);

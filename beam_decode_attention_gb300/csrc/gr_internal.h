@@ -83,6 +83,13 @@ cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 size_t select_list_bytes(int R, int W, int V, int next_width);
 int select_max_width();
 int select_max_beams();
+size_t trie_select_bytes(int R, int W, int next_width);
+cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_nodes, int num_edges,
+                               const float *logits, const float *beam_scores, const int32_t *beam_node,
+                               const int32_t *offsets, const int32_t *tokens, const int32_t *children,
+                               int32_t *next_parent, long long parent_stride, int32_t *next_token,
+                               float *next_score, int32_t *next_node, void *workspace, cudaStream_t s,
+                               cudaEvent_t between = nullptr);
 // `between` (may be null) is recorded on `s` between the two kernels
 cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float *logits,
                                const float *beam_scores, int32_t *next_parent, long long parent_stride,

@@ -477,6 +477,11 @@ struct MergeSelArgs {
     long long parent_stride;
     int32_t *next_token;
     float *next_score;
+    // item-constrained selection only (null otherwise): the trie and each
+    // beam's node, to give every kept beam its child node
+    const int32_t *beam_node, *trie_offsets, *trie_tokens, *trie_children;
+    int32_t *next_node;
+    int num_nodes, num_edges;
 };
 
 // dynamic shared memory of the merge kernel: list offsets, per-list counts
@@ -583,10 +588,13 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         j = e - offs[lo];
     };
     constexpr int kIn = 4;   // loads in flight per thread
-    // radix select of the next_width-th largest key
+    // radix select of the n_sel-th largest key (n_sel < next_width only when
+    // the request has fewer candidates: the rest of the slots are padding)
+    const int n_sel = min(a.next_width, total);
     uint32_t prefix = 0, mask = 0;
-    int need = a.next_width;
+    int need = n_sel;
     const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+    if (n_sel > 0) {
 #pragma unroll
     for (int rd = 0; rd < 3; ++rd) {
         for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
@@ -616,6 +624,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         prefix |= (bm - (uint32_t)(kHistBins - 1 - s_bin)) << sh;
         mask |= bm << sh;
         __syncthreads();
+    }
     }
     const uint32_t tau = prefix;   // need = how many entries equal to tau are taken
     // per list: entries above tau and tied with it (runs at the list's front)
@@ -664,15 +673,132 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     __syncthreads();
     int np2 = 1;
     while (np2 < a.next_width) np2 <<= 1;
-    for (int i = a.next_width + threadIdx.x; i < np2; i += blockDim.x) sel[i] = 0ull;
+    for (int i = n_sel + threadIdx.x; i < np2; i += blockDim.x) sel[i] = 0ull;
     __syncthreads();
     bitonic_desc(sel, np2);
     for (int j = threadIdx.x; j < a.next_width; j += blockDim.x) {
-        const unsigned long long e = sel[j];
-        const uint32_t flat = ~(uint32_t)e;
-        a.next_parent[(long long)r * a.parent_stride + j] = (int32_t)(flat / (uint32_t)a.V);
-        a.next_token[(long long)r * a.next_width + j] = (int32_t)(flat % (uint32_t)a.V);
-        a.next_score[(long long)r * a.next_width + j] = key_float((uint32_t)(e >> 32));
+        int32_t pb = -1, tv = -1, nd = -1;
+        float sc = -INFINITY;
+        if (j < n_sel) {
+            const unsigned long long e = sel[j];
+            const uint32_t flat = ~(uint32_t)e;
+            pb = (int32_t)(flat / (uint32_t)a.V);
+            tv = (int32_t)(flat % (uint32_t)a.V);
+            sc = key_float((uint32_t)(e >> 32));
+            if (a.next_node) {
+                // the edge of the parent's node that carries the token
+                const int n = a.beam_node[(long long)r * a.W + pb];
+                int lo = a.trie_offsets[n], hi = a.trie_offsets[n + 1];
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (a.trie_tokens[mid] < tv) lo = mid + 1;
+                    else hi = mid;
+                }
+                nd = a.trie_children[lo];
+            }
+        }
+        a.next_parent[(long long)r * a.parent_stride + j] = pb;
+        a.next_token[(long long)r * a.next_width + j] = tv;
+        a.next_score[(long long)r * a.next_width + j] = sc;
+        if (a.next_node) a.next_node[(long long)r * a.next_width + j] = nd;
+    }
+}
+
+// ---------------------------------------------------------------- item-constrained rows
+//
+// One CTA per beam row.  The row's legal tokens are the edges of its trie
+// node (CSR); their logits are gathered (pass A: maximum and sum of
+// exponentials over the legal tokens only, the log-normaliser of the masked
+// log_softmax), then scored in chunks of kTrieChunk edges that are sorted
+// together with the best entries so far, keeping the best min(W', degree)
+// by (score desc, token asc).  A node index or edge range outside the trie,
+// or an edge token outside [0, V), is skipped (nothing is read out of range).
+
+constexpr int kTrieThreads = 256;
+constexpr int kTrieChunk = 1024;
+
+struct TrieRowArgs {
+    const float *logits;
+    const float *beam_scores;
+    const int32_t *beam_node, *offsets, *tokens;
+    unsigned long long *lists;   // [R * W_s][W'] sorted descending
+    int *plen;
+    unsigned *tau_lb;
+    int rows, W, V, next_width, num_nodes, num_edges;
+};
+
+__global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) {
+    __shared__ unsigned long long buf[kMaxSel + kTrieChunk];
+    __shared__ MaxSum s_ms[kTrieThreads / 32];
+    __shared__ float s_c;
+    const int row = blockIdx.x;
+    const int n = a.beam_node[row];
+    int p0 = 0, p1 = 0;
+    if (n >= 0 && n < a.num_nodes) {
+        p0 = a.offsets[n];
+        p1 = a.offsets[n + 1];
+        if (p0 < 0 || p1 > a.num_edges || p1 < p0) p0 = p1 = 0;
+    }
+    const int deg = p1 - p0;
+    const float *z = a.logits + (long long)row * a.V;
+    const float S = a.beam_scores[row];
+    auto legal = [&](int k, int &v) {
+        v = a.tokens[p0 + k];
+        return v >= 0 && v < a.V;
+    };
+    // pass A: the log-normaliser over the legal logits
+    MaxSum ms{-INFINITY, 0.f};
+    for (int k = threadIdx.x; k < deg; k += blockDim.x) {
+        int v;
+        if (legal(k, v)) ms = ms_add(ms, __ldg(z + v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
+        ms = ms_merge(ms, other);
+    }
+    if ((threadIdx.x & 31) == 0) s_ms[threadIdx.x >> 5] = ms;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        MaxSum t = s_ms[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
+        s_c = t.m + __logf(t.s);
+    }
+    __syncthreads();
+    const float c = s_c;
+    // pass B: the best L entries, chunk by chunk
+    const int L = min(a.next_width, deg);
+    int cnt = 0;
+    for (int base = 0; base < deg; base += kTrieChunk) {
+        const int m = min(kTrieChunk, deg - base);
+        for (int k = threadIdx.x; k < m; k += blockDim.x) {
+            int v;
+            // a skipped edge sorts last and is not kept: key 0 is below every score
+            buf[cnt + k] = legal(base + k, v) ? pack(ord_key(score_of(__ldg(z + v), c, S)), ~(uint32_t)v) : 0ull;
+        }
+        const int tot = cnt + m;
+        int np2 = 1;
+        while (np2 < tot) np2 <<= 1;
+        for (int i = tot + threadIdx.x; i < np2; i += blockDim.x) buf[i] = 0ull;
+        __syncthreads();
+        bitonic_desc(buf, np2);
+        cnt = min(tot, L);
+    }
+    // drop skipped edges (key 0) from the kept count
+    __shared__ int s_keep;
+    if (threadIdx.x == 0) {
+        int k = cnt;
+        while (k > 0 && (buf[k - 1] >> 32) == 0ull) --k;
+        s_keep = k;
+    }
+    __syncthreads();
+    cnt = s_keep;
+    unsigned long long *out = a.lists + (long long)row * a.next_width;
+    for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = buf[j];
+    if (threadIdx.x == 0) {
+        a.plen[row] = cnt;
+        // a row with W' candidates of its own bounds the request's W'-th score
+        if (cnt == a.next_width && a.tau_lb) atomicMax(a.tau_lb + row / a.W, (unsigned)(buf[cnt - 1] >> 32));
     }
 }
 
@@ -742,7 +868,7 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     e = cudaGetLastError();
     if (e == cudaSuccess && between) e = cudaEventRecord(between, s);
     if (e != cudaSuccess) return e;
-    MergeSelArgs ma;
+    MergeSelArgs ma = {};
     ma.lists = ra.lists;
     ma.tau_lb = ra.tau_lb;
     ma.plen = counts;
@@ -754,6 +880,77 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ma.parent_stride = parent_stride;
     ma.next_token = next_token;
     ma.next_score = next_score;
+    select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
+    return cudaGetLastError();
+}
+
+size_t trie_select_bytes(int R, int W, int next_width) {
+    return list_bytes(R, W, next_width) + bound_bytes(R) + (size_t)R * W * sizeof(int);
+}
+
+cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_nodes, int num_edges,
+                               const float *logits, const float *beam_scores, const int32_t *beam_node,
+                               const int32_t *offsets, const int32_t *tokens, const int32_t *children,
+                               int32_t *next_parent, long long parent_stride, int32_t *next_token,
+                               float *next_score, int32_t *next_node, void *workspace, cudaStream_t s,
+                               cudaEvent_t between) {
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(select_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+    }
+    unsigned char *wsb = static_cast<unsigned char *>(workspace);
+    unsigned *tau_lb = reinterpret_cast<unsigned *>(wsb + list_bytes(R, W, next_width));
+    int *plen = reinterpret_cast<int *>(wsb + list_bytes(R, W, next_width) + bound_bytes(R));
+    e = cudaMemsetAsync(tau_lb, 0, (size_t)R * 4, s);
+    if (e != cudaSuccess) return e;
+    TrieRowArgs ta;
+    ta.logits = logits;
+    ta.beam_scores = beam_scores;
+    ta.beam_node = beam_node;
+    ta.offsets = offsets;
+    ta.tokens = tokens;
+    ta.lists = reinterpret_cast<unsigned long long *>(wsb);
+    ta.plen = plen;
+    ta.tau_lb = tau_lb;
+    ta.rows = R * W;
+    ta.W = W;
+    ta.V = V;
+    ta.next_width = next_width;
+    ta.num_nodes = num_nodes;
+    ta.num_edges = num_edges;
+    trie_rows_kernel<<<R * W, kTrieThreads, 0, s>>>(ta);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && between) e = cudaEventRecord(between, s);
+    if (e != cudaSuccess) return e;
+    MergeSelArgs ma = {};
+    ma.lists = ta.lists;
+    ma.tau_lb = tau_lb;
+    ma.plen = plen;
+    ma.W = W;
+    ma.V = V;
+    ma.L = next_width;
+    ma.next_width = next_width;
+    ma.next_parent = next_parent;
+    ma.parent_stride = parent_stride;
+    ma.next_token = next_token;
+    ma.next_score = next_score;
+    ma.beam_node = beam_node;
+    ma.trie_offsets = offsets;
+    ma.trie_tokens = tokens;
+    ma.trie_children = children;
+    ma.next_node = next_node;
+    ma.num_nodes = num_nodes;
+    ma.num_edges = num_edges;
     select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
     return cudaGetLastError();
 }

@@ -55,7 +55,7 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["attention", "beam_select"], default="attention")
+    p.add_argument("--op", choices=["attention", "beam_select", "trie_select"], default="attention")
     return p.parse_args()
 
 
@@ -366,6 +366,85 @@ def run_select_bench(args):
     return 0
 
 
+TRIE_METRIC = ("µs per item-constrained selection call (R=4, W=900->900, V=151936, SID trie of 200k items, "
+               "3 levels x 256 codes); % of HBM roofline")
+
+
+def run_trie_bench(args):
+    """Item-constrained selection (gr_trie_select): beams at trie level 1,
+    so every beam has up to 256 legal tokens."""
+    import torch
+    import beam_decode_attention_gb300 as gr
+    cfg = workloads.SELECT_TRIE_HEADLINE
+    R, W, V, n = cfg["num_requests"], cfg["width"], cfg["vocab"], cfg["next_width"]
+    trie = workloads.make_sid_trie(cfg["items"], cfg["levels"], cfg["codebook"], V, seed=31)
+    inp = workloads.make_trie_select_inputs(R, W, V, trie, cfg["level"], seed=32)
+    degs = np.diff(trie["offsets"])[inp["beam_node"]]
+    legal = int(degs.sum())
+    conf = {"workload": "trie_select_r4_w900_v151936_sid3x256", **cfg,
+            "legal_candidates": legal, "l2": "logits 2.19 GB, of which only the legal entries are read; no flush"}
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        from oracle import select
+        t0 = time.perf_counter()
+        select.trie_select(inp["logits"][:1], inp["beam_scores"][:1], inp["beam_node"][:1], trie["offsets"],
+                           trie["tokens"], trie["children"], n)
+        value = (time.perf_counter() - t0) * R * 1e6
+        print(json.dumps({
+            "impl": "reference", "metric": TRIE_METRIC, "value": value, "unit": SELECT_UNIT, "n_gpus": 1,
+            "steps": 1, "warmup": 0, "ms_per_step": value / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": conf,
+            "cpu_baseline": {"value": value, "unit": SELECT_UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"request 0 of {R}, time scaled by {R}"},
+            "e2e": {"value": value, "unit": SELECT_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
+    torch.cuda.set_device(0)
+    gr.load()
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    logits, scores, bn = d(inp["logits"]), d(inp["beam_scores"]), d(inp["beam_node"])
+    off, tok, ch = d(trie["offsets"]), d(trie["tokens"]), d(trie["children"])
+    shape = gr.TrieSelectShape(R, W, V, n, trie["num_nodes"], len(trie["tokens"]))
+    ws = torch.empty(gr.gr_trie_select_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    par = torch.empty((R, n), dtype=torch.int32, device="cuda")
+    tk, nd = torch.empty_like(par), torch.empty_like(par)
+    sc = torch.empty((R, n), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        gr.gr_trie_select(shape, logits, scores, bn, off, tok, ch, par, tk, sc, nd, ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    clocks.start()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()   # the legal logits are a few MB: flush L2 before each call
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gr.gr_trie_select(shape, logits, scores, bn, off, tok, ch, par, tk, sc, nd, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000.0)
+    clk = clocks.stop()
+    value = float(np.mean(times))
+    pk = peaks()
+    # algorithmic bytes: the legal logits, their edge tokens and children, the
+    # beams' nodes, scores and trie offsets, and the outputs
+    alg = legal * 4 * 3 + R * W * 12 + R * n * 16
+    conf["l2"] = "flushed (256 MB buffer written) before every timed call"
+    line = {
+        "metric": TRIE_METRIC, "value": value, "unit": SELECT_UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": value / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": conf,
+        "roofline": {"bound": "hbm", "achieved": round(alg / (value * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(alg / (value * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                     "traffic": None, "kernel": "whole call (trie_rows_kernel + select_merge_kernel)",
+                     "peak_source": pk.get("source", "measured copy")},
+        "gpu_launches": 2 * args.steps, "clocks": clk, "cpu_baseline": None, "e2e": None,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.gpus != 1:
@@ -373,6 +452,8 @@ def main():
         return 2
     if args.op == "beam_select":
         return run_select_bench(args)
+    if args.op == "trie_select":
+        return run_trie_bench(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

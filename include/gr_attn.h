@@ -278,6 +278,59 @@ int gr_beam_select_timed(const gr_select_shape *shape, const float *logits,
                          int32_t *next_token, float *next_score, void *workspace,
                          size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events);
 
+/*
+ * Item-constrained beam selection (GR-Inference blog, "kernel design": the
+ * item-constrained fused kernel with the SID trie resident on the device in
+ * CSR form, prefix traversal, legal-token gather and a local top-K, and no
+ * full-vocabulary mask; xGR review, "xBeam": an item mask on the logits).
+ *
+ * The trie: node n's edges are k in [trie_offsets[n], trie_offsets[n+1]),
+ * each with a token trie_tokens[k] (strictly increasing within a node, in
+ * [0, V)) and a child node trie_children[k]; node 0 is the root.  Beam b of
+ * request r sits at node beam_node[r, b] (the root at the first step).  Its
+ * legal next tokens are its node's edge tokens, and the log_softmax is taken
+ * over those only (every other logit masked):
+ *     score[r, b, k] = beam_scores[r, b] + logits[r, b, t_k]
+ *                      - ln sum_{k' edges of the node} exp(logits[r, b, t_k'])
+ * The next_width candidates of largest score are kept exactly as
+ * gr_beam_select keeps them (equal scores by the smaller b * V + token), and
+ * next_node[r * next_width + j] is the chosen edge's child, so each step
+ * advances the traversal one level.  A beam at a leaf has no candidates;
+ * slots past a request's candidates get parent -1, token -1, score -inf and
+ * node -1.  A node index, edge range or token out of range is skipped
+ * (nothing is read out of it).
+ */
+typedef struct {
+    int32_t num_requests; /* R >= 1 */
+    int32_t width;        /* W_s: 1 <= W_s <= GR_SELECT_MAX_BEAMS */
+    int32_t vocab;        /* V >= 1; W_s * V < 2^31 */
+    int32_t next_width;   /* W': 1 <= W' <= GR_SELECT_MAX_WIDTH */
+    int32_t num_nodes;    /* N >= 1 trie nodes */
+    int32_t num_edges;    /* E >= 0 trie edges */
+} gr_trie_select_shape;
+
+/* Bytes of device workspace gr_trie_select needs (0 on a bad shape). */
+size_t gr_trie_select_workspace_size(const gr_trie_select_shape *shape);
+
+/*
+ *   logits, beam_scores   as for gr_beam_select
+ *   beam_node             device int32 [R, W_s]
+ *   trie_offsets          device int32 [N + 1]
+ *   trie_tokens           device int32 [E]
+ *   trie_children         device int32 [E]
+ *   next_parent           as for gr_beam_select (row stride parent_stride)
+ *   next_token, next_node device int32 [R, next_width], written
+ *   next_score            device fp32 [R, next_width], written
+ * Device pointers must be 16-byte aligned (trie_tokens / trie_children may be
+ * NULL when E = 0).  Two kernels on `stream`; nothing is allocated.  Errors
+ * as for gr_beam_select.
+ */
+int gr_trie_select(const gr_trie_select_shape *shape, const float *logits, const float *beam_scores,
+                   const int32_t *beam_node, const int32_t *trie_offsets, const int32_t *trie_tokens,
+                   const int32_t *trie_children, int32_t *next_parent, int64_t parent_stride,
+                   int32_t *next_token, float *next_score, int32_t *next_node, void *workspace,
+                   size_t workspace_bytes, gr_stream_t stream);
+
 /* Static description of a gr_status code. */
 const char *gr_status_string(int status);
 

@@ -148,3 +148,28 @@ def test_beam_select_rejects_bad_args(lib):
     assert call(logits=FAKE + 4) == -4
     assert call(token=FAKE + 8) == -4
     assert call(ws_bytes=_sel_bytes(2, 4, 100, 8) - 1) == -5
+
+
+def _tsel(**kw):
+    d = dict(num_requests=2, width=4, vocab=100, next_width=8, num_nodes=10, num_edges=9)
+    d.update(kw)
+    return gr.TrieSelectShape(*[d[k] for k in ("num_requests", "width", "vocab", "next_width",
+                                                  "num_nodes", "num_edges")])
+
+
+def test_trie_select_workspace_and_bad_args(lib):
+    # per beam row a list of next_width 8-byte entries and its length; a bound per request
+    assert lib.gr_trie_select_workspace_size(ctypes.byref(_tsel())) == 2 * 4 * 8 * 8 + 16 + 2 * 4 * 4
+    for bad in (dict(num_nodes=0), dict(num_edges=-1), dict(next_width=1025), dict(width=4097)):
+        assert lib.gr_trie_select_workspace_size(ctypes.byref(_tsel(**bad))) == 0, bad
+
+    def call(shape=ctypes.byref(_tsel()), toks=FAKE, node_out=FAKE, stride=8, ws_bytes=1 << 20, logits=FAKE):
+        return lib.gr_trie_select(shape, logits, FAKE, FAKE, FAKE, toks, FAKE, FAKE, stride, FAKE, FAKE,
+                                  node_out, FAKE, ws_bytes, None)
+
+    assert call(shape=None) == -1
+    assert call(toks=None) == -1
+    assert call(node_out=None) == -1
+    assert call(stride=7) == -2
+    assert call(logits=FAKE + 4) == -4
+    assert call(ws_bytes=10) == -5

@@ -1,0 +1,120 @@
+"""Parity of gr_trie_select (item-constrained beam selection, through the C
+ABI) with its oracle: a hand-worked trie, random SID tries at every level
+(leaves, padding), a node with more edges than one chunk, out-of-range trie
+indices, and the measured size on two requests."""
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import select
+import test_oracle_trie_select as hand
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():   # pragma: no cover - CPU-only machines
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import beam_decode_attention_gb300 as gr  # noqa: E402
+
+TOL = 1e-4
+
+
+def dev(a, dtype=None):
+    return torch.from_numpy(np.ascontiguousarray(a if dtype is None else a.astype(dtype))).cuda()
+
+
+def run(logits, scores, beam_node, offsets, tokens, children, n, num_nodes=None):
+    R, W, V = logits.shape
+    N = len(offsets) - 1 if num_nodes is None else num_nodes
+    shape = gr.TrieSelectShape(R, W, V, n, N, len(tokens))
+    ws = torch.empty(max(16, gr.gr_trie_select_workspace_size(shape)), dtype=torch.uint8, device="cuda")
+    par = torch.empty((R, n), dtype=torch.int32, device="cuda")
+    tok = torch.empty_like(par)
+    nod = torch.empty_like(par)
+    sco = torch.empty((R, n), dtype=torch.float32, device="cuda")
+    tk = dev(tokens, np.int32) if len(tokens) else torch.zeros(4, dtype=torch.int32, device="cuda")
+    ch = dev(children, np.int32) if len(children) else torch.zeros(4, dtype=torch.int32, device="cuda")
+    gr.gr_trie_select(shape, dev(logits, np.float32), dev(scores, np.float32), dev(beam_node, np.int32),
+                      dev(offsets, np.int32), tk, ch, par, tok, sco, nod, ws)
+    torch.cuda.synchronize()
+    return par.cpu().numpy(), tok.cpu().numpy(), nod.cpu().numpy(), sco.cpu().numpy()
+
+
+def check(logits, scores, beam_node, offsets, tokens, children, n, got, requests=None):
+    par, tok, nod, sco = got
+    rp, rt, rn, rs = select.trie_select(logits, scores, beam_node, offsets, tokens, children, n)
+    R, W, V = logits.shape
+    for r in (range(R) if requests is None else requests):
+        real = rp[r] >= 0
+        k = int(real.sum())
+        # padding where the oracle has no candidate
+        assert np.all(par[r, k:] == -1) and np.all(tok[r, k:] == -1) and np.all(nod[r, k:] == -1)
+        assert np.all(np.isneginf(sco[r, k:]))
+        assert np.allclose(sco[r, :k], rs[r, :k], rtol=0, atol=TOL * max(1.0, np.abs(rs[r, :k]).max(initial=0)))
+        gaps = -np.diff(rs[r, :k])
+        if k <= 1 or np.all(gaps > 2 * TOL * max(1.0, np.abs(rs[r, :k]).max())):
+            assert np.array_equal(par[r, :k], rp[r, :k]) and np.array_equal(tok[r, :k], rt[r, :k])
+            assert np.array_equal(nod[r, :k], rn[r, :k])
+        else:
+            # near-ties: same multiset of candidates up to the tolerance, each pick a real edge
+            got_flat = set(zip(par[r, :k].tolist(), tok[r, :k].tolist()))
+            clear = [(p, t) for p, t, s in zip(rp[r, :k], rt[r, :k], rs[r, :k]) if s > rs[r, k - 1] + 2 * TOL]
+            assert set(clear) <= got_flat
+            for p, t, c in zip(par[r, :k], tok[r, :k], nod[r, :k]):
+                nd = beam_node[r, p]
+                e = np.arange(offsets[nd], offsets[nd + 1])
+                assert t in tokens[e] and c == children[e[np.searchsorted(tokens[e], t)]]
+
+
+def test_hand_worked_trie():
+    d = hand.hand_case()
+    got = run(d["logits"].astype(np.float32), d["S"].astype(np.float32), d["beam_node"], d["offsets"],
+              d["tokens"], d["children"], d["n"])
+    want = d["want"]
+    assert [int(x) for x in got[0][0]] == [w[0] for w in want]
+    assert [int(x) for x in got[1][0]] == [w[1] for w in want]
+    assert [int(x) for x in got[2][0]] == [w[2] for w in want]
+    assert np.allclose(got[3][0][:3], [w[3] for w in want[:3]], atol=1e-6) and np.isneginf(got[3][0][3])
+
+
+@pytest.mark.parametrize("level,W,n", [(0, 5, 7), (1, 16, 40), (2, 30, 64), (3, 4, 5), (1, 3, 200)])
+def test_random_sid_tries(level, W, n):
+    t = workloads.make_sid_trie(3000, 3, 24, 500, seed=level * 10 + W)
+    inp = workloads.make_trie_select_inputs(2, W, 500, t, level, seed=level + W + n)
+    got = run(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], n)
+    check(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], n, got)
+
+
+def test_node_with_more_edges_than_a_chunk():
+    t = workloads.make_sid_trie(8000, 1, 3000, 4000, seed=77)   # the root has ~2800 edges
+    assert t["offsets"][1] > 2048
+    inp = workloads.make_trie_select_inputs(2, 6, 4000, t, 0, seed=78)
+    got = run(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], 1000)
+    check(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], 1000, got)
+
+
+def test_out_of_range_nodes_are_skipped():
+    """Beams whose node index lies outside the trie contribute nothing (the
+    kernel checks the index before reading the trie)."""
+    t = workloads.make_sid_trie(500, 2, 10, 100, seed=5)
+    inp = workloads.make_trie_select_inputs(1, 6, 100, t, 1, seed=6)
+    bn = inp["beam_node"].copy()
+    bn[0, 1] = -5
+    bn[0, 4] = t["num_nodes"] + 3
+    got = run(inp["logits"], inp["beam_scores"], bn, t["offsets"], t["tokens"], t["children"], 12)
+    keep = bn.copy()
+    leaf = t["level_nodes"][-1][0]          # a leaf stands in for the skipped beams in the oracle
+    keep[0, 1] = keep[0, 4] = leaf
+    check(inp["logits"], inp["beam_scores"], keep, t["offsets"], t["tokens"], t["children"], 12, got)
+
+
+def test_headline_size_sampled_requests():
+    cfg = workloads.SELECT_TRIE_HEADLINE
+    t = workloads.make_sid_trie(cfg["items"], cfg["levels"], cfg["codebook"], cfg["vocab"], seed=31)
+    inp = workloads.make_trie_select_inputs(cfg["num_requests"], cfg["width"], cfg["vocab"], t, cfg["level"], seed=32)
+    got = run(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"],
+              cfg["next_width"])
+    check(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"],
+          cfg["next_width"], got, requests=[0, 3])

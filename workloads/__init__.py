@@ -216,3 +216,59 @@ def make_select_inputs(num_requests: int, width: int, vocab: int, seed: int,
     scores = (-np.abs(rng.standard_normal(size=(num_requests, width), dtype=np.float32))
               * np.float32(3.0))
     return dict(logits=logits, beam_scores=scores)
+
+
+# --------------------------------------------------------------------------- item-constrained selection
+#
+# A synthetic SID catalogue: `items` items, each a path of `levels` codes in
+# [0, codebook) drawn uniformly (Generator(PCG64(seed))); the codes of level l
+# are the vocabulary tokens token_base + l * codebook + code (the SID tokens
+# sit at the end of the vocabulary).  The trie of the distinct paths is
+# returned in CSR form with nodes numbered level by level (root 0), each
+# node's edges sorted by token.
+
+SELECT_TRIE_HEADLINE = dict(num_requests=4, width=900, vocab=151936, next_width=900,
+                            codebook=256, levels=3, items=200_000, level=1)
+
+
+def make_sid_trie(items: int, levels: int, codebook: int, vocab: int, seed: int):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    codes = rng.integers(0, codebook, size=(items, levels), dtype=np.int64)
+    token_base = vocab - levels * codebook
+    if token_base < 0:
+        raise ValueError("vocabulary smaller than the SID tokens")
+    # nodes level by level: the distinct prefixes of each length
+    level_nodes = [np.array([0])]
+    prefix_id = {(): 0}
+    edges = {}   # node -> list of (token, child)
+    next_id = 1
+    for lv in range(levels):
+        prefixes = np.unique(codes[:, :lv + 1], axis=0)
+        ids = []
+        for p in map(tuple, prefixes):
+            parent = prefix_id[p[:-1]]
+            prefix_id[p] = next_id
+            edges.setdefault(parent, []).append((int(token_base + lv * codebook + p[-1]), next_id))
+            ids.append(next_id)
+            next_id += 1
+        level_nodes.append(np.array(ids))
+    offsets = np.zeros(next_id + 1, np.int32)
+    tokens, children = [], []
+    for n in range(next_id):
+        for t, c in sorted(edges.get(n, [])):
+            tokens.append(t)
+            children.append(c)
+        offsets[n + 1] = len(tokens)
+    return dict(offsets=offsets, tokens=np.array(tokens, np.int32), children=np.array(children, np.int32),
+                num_nodes=next_id, level_nodes=level_nodes)
+
+
+def make_trie_select_inputs(num_requests: int, width: int, vocab: int, trie, level: int, seed: int,
+                            logit_std: float = 2.0) -> Dict[str, np.ndarray]:
+    """Logits and beam scores as make_select_inputs, plus each beam's trie
+    node: a uniformly drawn node of the given level (0 = the root)."""
+    d = make_select_inputs(num_requests, width, vocab, seed, logit_std)
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    nodes = trie["level_nodes"][level]
+    d["beam_node"] = nodes[rng.integers(0, len(nodes), size=(num_requests, width))].astype(np.int32)
+    return d
