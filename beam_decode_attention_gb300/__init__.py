@@ -32,7 +32,8 @@ __all__ = [
     "gr_version", "EXPORTED_SYMBOLS", "gr_decode_attn_timed", "gr_decode_attn_plan", "PlanInfo",
     "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES", "SelectShape", "gr_beam_select",
     "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
-    "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size",
+    "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size", "CtxPages",
+    "gr_decode_attn_paged",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -40,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
     "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
-    "gr_trie_select_workspace_size", "gr_trie_select",
+    "gr_trie_select_workspace_size", "gr_trie_select", "gr_decode_attn_paged",
 )
 
 # GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
@@ -105,6 +106,15 @@ class TrieSelectShape(ctypes.Structure):
     ]
 
 
+class CtxPages(ctypes.Structure):
+    """``gr_ctx_pages``."""
+    _fields_ = [
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("pages_per_request", ctypes.c_int32),
+    ]
+
+
 class PlanInfo(ctypes.Structure):
     """``gr_plan_info``."""
     _fields_ = [
@@ -146,6 +156,9 @@ def load() -> ctypes.CDLL:
     lib.gr_decode_attn_timed.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz,
                                          vp, vp]
     lib.gr_decode_attn_timed.restype = ctypes.c_int
+    lib.gr_decode_attn_paged.argtypes = [sp, ctypes.POINTER(CtxPages), vp, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, i32, vp, vp, vp, sz, vp]
+    lib.gr_decode_attn_paged.restype = ctypes.c_int
     lib.gr_decode_attn_plan.argtypes = [sp, vp, i32, ctypes.POINTER(PlanInfo)]
     lib.gr_decode_attn_plan.restype = ctypes.c_int
     lib.gr_decode_attn_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
@@ -232,6 +245,20 @@ def gr_decode_attn(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_
                                int(step), _ptr(out), _ptr(lse), _ptr(workspace),
                                int(workspace_bytes), _stream_handle(stream))
     _check(rc, "gr_decode_attn")
+
+
+def gr_decode_attn_paged(shape: Shape, pages: CtxPages, q, ctx_k_pool, ctx_v_pool, ctx_len, block_table,
+                         beam_k, beam_v, beam_path, widths: Sequence[int], step: int, out, lse,
+                         workspace=None, workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """gr_decode_attn over a paged ContextKV pool (see ``include/gr_attn.h``)."""
+    w = _widths_arr(widths)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().gr_decode_attn_paged(ctypes.byref(shape), ctypes.byref(pages), _ptr(q), _ptr(ctx_k_pool),
+                                     _ptr(ctx_v_pool), _ptr(ctx_len), _ptr(block_table), _ptr(beam_k),
+                                     _ptr(beam_v), _ptr(beam_path), w, int(step), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), int(workspace_bytes), _stream_handle(stream))
+    _check(rc, "gr_decode_attn_paged")
 
 
 def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,

@@ -133,6 +133,22 @@ __device__ __forceinline__ bool wait_lane(uint32_t bar, uint32_t parity, volatil
     return true;
 }
 
+// Tensor-map coordinates (position, request-or-page) of context key `key`
+// of request r: the dense layout [R, Hkv, Lc_max, D], or a paged pool
+// [num_pages, Hkv, page_size, D] through the request's block table (page
+// sizes are multiples of the 128-key block, so a block never straddles two
+// pages).  A page index outside the pool lands outside the tensor map, where
+// TMA reads zeros.
+__device__ __forceinline__ void kv_coords(const CtxArgs &a, int r, int key, int &c1, int &c3) {
+    if (a.page_size == 0) {
+        c1 = key;
+        c3 = r;
+    } else {
+        c1 = key % a.page_size;
+        c3 = a.block_table[(long long)r * a.pages_per_req + key / a.page_size];
+    }
+}
+
 // One query row of the per-beam stage: its chain is walked by beam_prologue.
 struct BeamRow {
     bool valid;      // a row of this call (inside the tile and the step's width)
@@ -404,9 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      h * 64, kvh * g.G, (tile0 + t) * p.bpt, r);
             // load 0 (K of block 0) into ring slot 0, which starts out free
             ptx::mbar_arrive_expect_tx(bar(kBarKvFull + 0), (uint32_t)C::kTileBytes);
+            int c1, c3;
+            kv_coords(p.a, r, kbeg, c1, c3);
             for (int h = 0; h < C::kHalves; ++h)
-                ptx::tma_load_4d(sbase + C::kKvOff + h * C::kHalfBytes, &tm_k, bar(kBarKvFull + 0), h * 64, kbeg, kvh,
-                                 r);
+                ptx::tma_load_4d(sbase + C::kKvOff + h * C::kHalfBytes, &tm_k, bar(kBarKvFull + 0), h * 64, c1, kvh,
+                                 c3);
         }
         __syncwarp();
     }
@@ -439,10 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(bar(kBarKvFull + s), (uint32_t)C::kTileBytes);
                     const CUtensorMap *tm = (n & 1) ? &tm_v : &tm_k;
-                    const int key = kbeg + (n >> 1) * kBN;
+                    int c1, c3;
+                    kv_coords(p.a, r, kbeg + (n >> 1) * kBN, c1, c3);
                     for (int h = 0; h < C::kHalves; ++h)
                         ptx::tma_load_4d(sbase + C::kKvOff + s * C::kTileBytes + h * C::kHalfBytes, tm,
-                                         bar(kBarKvFull + s), h * 64, key, kvh, r);
+                                         bar(kBarKvFull + s), h * 64, c1, kvh, c3);
                 }
                 __syncwarp();
                 issued = n + 1;
@@ -821,8 +840,11 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
     const uint64_t qd[4] = {(uint64_t)D, (uint64_t)g.Hq, (uint64_t)g.W_s, (uint64_t)g.R};
     const uint64_t qs[3] = {(uint64_t)D * 2, (uint64_t)g.Hq * D * 2, (uint64_t)g.W_s * g.Hq * D * 2};
     const uint32_t qb[4] = {64, (uint32_t)g.G, (uint32_t)bpt, 1};
-    const uint64_t kd[4] = {(uint64_t)D, (uint64_t)g.Lc_max, (uint64_t)g.Hkv, (uint64_t)g.R};
-    const uint64_t ks[3] = {(uint64_t)D * 2, (uint64_t)g.Lc_max * D * 2, (uint64_t)g.Hkv * g.Lc_max * D * 2};
+    // dense [R, Hkv, Lc_max, D] or a paged pool [num_pages, Hkv, page_size, D]
+    const uint64_t rows = a.page_size ? (uint64_t)a.page_size : (uint64_t)g.Lc_max;
+    const uint64_t outer = a.page_size ? (uint64_t)a.num_pages : (uint64_t)g.R;
+    const uint64_t kd[4] = {(uint64_t)D, rows, (uint64_t)g.Hkv, outer};
+    const uint64_t ks[3] = {(uint64_t)D * 2, rows * D * 2, (uint64_t)g.Hkv * rows * D * 2};
     const uint32_t kb[4] = {64, (uint32_t)kBN, 1, 1};
     if (!encode_4d(&tq, a.q, qd, qs, qb) || !encode_4d(&tk, a.ctx_k, kd, ks, kb) ||
         !encode_4d(&tv, a.ctx_v, kd, ks, kb))

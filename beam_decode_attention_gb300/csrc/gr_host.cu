@@ -247,10 +247,20 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
                const int32_t *ctx_len, const void *beam_k, const void *beam_v,
                const int32_t *beam_path, const int32_t *widths, int32_t step, void *out, float *lse,
                void *workspace, size_t workspace_bytes, gr_stream_t stream,
-               gr_event_t const *events) {
+               gr_event_t const *events, const gr_ctx_pages *pages = nullptr,
+               const int32_t *block_table = nullptr) {
     Geometry g;
     int rc = make_geometry(shape, widths, step, &g);
     if (rc != GR_OK) return rc;
+    if (pages) {
+        if (pages->page_size < 128 || pages->page_size % 128 != 0 || pages->num_pages < 1 ||
+            pages->pages_per_request < 1 ||
+            (long long)pages->pages_per_request * pages->page_size < (long long)g.Lc_max)
+            return GR_ERR_BAD_SHAPE;
+        if (!block_table) return GR_ERR_NULL_ARG;
+        if (misaligned(block_table)) return GR_ERR_MISALIGNED;
+        if (chosen_path() == Path::kSimt) return GR_ERR_UNSUPPORTED;   // the cross-check path reads dense only
+    }
     if (!q || !ctx_len || !beam_k || !beam_v || !beam_path || !out || !lse) return GR_ERR_NULL_ARG;
     if (g.Lc_max > 0 && (!ctx_k || !ctx_v)) return GR_ERR_NULL_ARG;
     if (misaligned(q) || misaligned(ctx_k) || misaligned(ctx_v) || misaligned(ctx_len) ||
@@ -291,6 +301,12 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         c.beam_path = beam_path;
         c.out = static_cast<uint16_t *>(out);
         c.lse = lse;
+        if (pages) {
+            c.block_table = block_table;
+            c.page_size = pages->page_size;
+            c.pages_per_req = pages->pages_per_request;
+            c.num_pages = pages->num_pages;
+        }
         rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
         if (rc != GR_OK) return rc;
     }
@@ -323,6 +339,16 @@ int gr_decode_attn(const gr_attn_shape *shape, const void *q, const void *ctx_k,
                    float *lse, void *workspace, size_t workspace_bytes, gr_stream_t stream) {
     return run_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
                       lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+int gr_decode_attn_paged(const gr_attn_shape *shape, const gr_ctx_pages *pages, const void *q,
+                         const void *ctx_k_pool, const void *ctx_v_pool, const int32_t *ctx_len,
+                         const int32_t *block_table, const void *beam_k, const void *beam_v,
+                         const int32_t *beam_path, const int32_t *widths, int32_t step, void *out,
+                         float *lse, void *workspace, size_t workspace_bytes, gr_stream_t stream) {
+    if (!pages) return GR_ERR_NULL_ARG;
+    return run_decode(shape, q, ctx_k_pool, ctx_v_pool, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
+                      lse, workspace, workspace_bytes, stream, nullptr, pages, block_table);
 }
 
 int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *ctx_k,

@@ -51,6 +51,11 @@ struct CtxArgs {
     const int32_t *beam_path;
     uint16_t *out;
     float *lse;
+    // paged ContextKV (page_size 0: the dense [R, Hkv, Lc_max, D] layout):
+    // position j of request r sits in page block_table[r * pages_per_req +
+    // j / page_size] of a pool [num_pages, Hkv, page_size, D], at j % page_size
+    const int32_t *block_table = nullptr;
+    int page_size = 0, pages_per_req = 0, num_pages = 0;
 };
 
 struct MergeArgs {

@@ -113,6 +113,33 @@ int gr_decode_attn(const gr_attn_shape *shape, const void *q, const void *ctx_k,
                    size_t workspace_bytes, gr_stream_t stream);
 
 /*
+ * Paged ContextKV (SID-GR README, section 10 "TODO and Roadmap": page-backed
+ * ContextKV storage and native page tables in decode attention).  The
+ * context of request r is a list of pages of a shared pool:
+ *     position j of request r  ->  page block_table[r * pages_per_request + j / page_size],
+ *                                  offset j % page_size
+ *     ctx_k_pool, ctx_v_pool   device bf16 [num_pages, Hkv, page_size, D]
+ *     block_table              device int32 [R, pages_per_request]
+ * Only the pages that cover positions below ctx_len[r] are read.  A page
+ * index outside [0, num_pages) reads zeros (it is not followed out of the
+ * pool).  Everything else -- shapes, outputs, workspace (same size as
+ * gr_decode_attn for the same shape), errors -- is as for gr_decode_attn, with
+ * ctx_capacity <= pages_per_request * page_size.  The CUDA-core cross-check
+ * path (GR_ATTN_FORCE_PATH=simt) does not take pages: GR_ERR_UNSUPPORTED.
+ */
+typedef struct {
+    int32_t page_size;          /* positions per page: a positive multiple of 128 */
+    int32_t num_pages;          /* pages in the pool, >= 1 */
+    int32_t pages_per_request;  /* block-table row length */
+} gr_ctx_pages;
+
+int gr_decode_attn_paged(const gr_attn_shape *shape, const gr_ctx_pages *pages, const void *q,
+                         const void *ctx_k_pool, const void *ctx_v_pool, const int32_t *ctx_len,
+                         const int32_t *block_table, const void *beam_k, const void *beam_v,
+                         const int32_t *beam_path, const int32_t *widths, int32_t step, void *out,
+                         float *lse, void *workspace, size_t workspace_bytes, gr_stream_t stream);
+
+/*
  * Size of the static device scratch gr_decode_attn_noalloc uses: 64 MiB.
  */
 #define GR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
