@@ -33,7 +33,7 @@ __all__ = [
     "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES", "SelectShape", "gr_beam_select",
     "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
     "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size", "CtxPages",
-    "gr_decode_attn_paged",
+    "gr_decode_attn_paged", "gr_beam_reorder",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "gr_decode_attn_plan", "gr_resolve_ancestors", "gr_validate_beam_path",
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
     "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
-    "gr_trie_select_workspace_size", "gr_trie_select", "gr_decode_attn_paged",
+    "gr_trie_select_workspace_size", "gr_trie_select", "gr_decode_attn_paged", "gr_beam_reorder",
 )
 
 # GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
@@ -179,6 +179,8 @@ def load() -> ctypes.CDLL:
     lib.gr_trie_select_workspace_size.restype = sz
     lib.gr_trie_select.argtypes = [tsp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz, vp]
     lib.gr_trie_select.restype = ctypes.c_int
+    lib.gr_beam_reorder.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.gr_beam_reorder.restype = ctypes.c_int
     lib.gr_get_device_error.argtypes = []
     lib.gr_get_device_error.restype = ctypes.c_int
     lib.gr_status_string.argtypes = [ctypes.c_int]
@@ -381,6 +383,15 @@ def gr_trie_select(shape: TrieSelectShape, logits, beam_scores, beam_node, trie_
                                _ptr(next_score), _ptr(next_node), _ptr(workspace), int(workspace_bytes),
                                _stream_handle(stream))
     _check(rc, "gr_trie_select")
+
+
+def gr_beam_reorder(shape: Shape, beam_k, beam_v, beam_path, widths: Sequence[int], step: int,
+                    out_k, out_v, out_path, stream=None) -> None:
+    """The per-beam cache reordered along BeamPath (see ``include/gr_attn.h``)."""
+    rc = load().gr_beam_reorder(ctypes.byref(shape), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path),
+                                _widths_arr(widths), int(step), _ptr(out_k), _ptr(out_v), _ptr(out_path),
+                                _stream_handle(stream))
+    _check(rc, "gr_beam_reorder")
 
 
 def gr_get_device_error() -> int:

@@ -493,6 +493,25 @@ int gr_trie_select(const gr_trie_select_shape *shape, const float *logits, const
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int gr_beam_reorder(const gr_attn_shape *shape, const void *beam_k, const void *beam_v, const int32_t *beam_path,
+                    const int32_t *widths, int32_t step, void *out_k, void *out_v, int32_t *out_path,
+                    gr_stream_t stream) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!beam_k || !beam_v || !beam_path || !out_k || !out_v || !out_path) return GR_ERR_NULL_ARG;
+    if (misaligned(beam_k) || misaligned(beam_v) || misaligned(beam_path) || misaligned(out_k) ||
+        misaligned(out_v) || misaligned(out_path))
+        return GR_ERR_MISALIGNED;
+    if (out_k == beam_k || out_v == beam_v) return GR_ERR_BAD_SHAPE;   // out of place only
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_reorder(g, static_cast<const uint16_t *>(beam_k), static_cast<const uint16_t *>(beam_v),
+                                      beam_path, static_cast<uint16_t *>(out_k), static_cast<uint16_t *>(out_v),
+                                      out_path, dev.err_ptr, static_cast<cudaStream_t>(stream)));
+}
+
 int gr_get_device_error(void) {
     DeviceInfo dev;
     int rc = device_info(&dev);

@@ -84,6 +84,11 @@ int tc_beams_per_tile(int G);
 int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 
+// gr_reorder.cu  (per-beam cache reordered along BeamPath)
+cudaError_t launch_reorder(const Geometry &g, const uint16_t *beam_k, const uint16_t *beam_v,
+                           const int32_t *beam_path, uint16_t *out_k, uint16_t *out_v, int32_t *out_path, int *err,
+                           cudaStream_t s);
+
 // gr_select.cu  (beam selection)
 size_t select_list_bytes(int R, int W, int V, int next_width);
 int select_max_width();

@@ -55,7 +55,7 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["attention", "beam_select", "trie_select"], default="attention")
+    p.add_argument("--op", choices=["attention", "beam_select", "trie_select", "reorder"], default="attention")
     return p.parse_args()
 
 
@@ -445,6 +445,66 @@ def run_trie_bench(args):
     return 0
 
 
+def run_reorder_bench(args):
+    """BeamPath indirection against the reordered per-beam cache (xGR's
+    alternative) on the headline workload: per decode step, the attention
+    call through BeamPath, against gr_beam_reorder plus the attention call on
+    the reordered cache with the identity path.  L2 flushed before each call."""
+    import torch
+    import beam_decode_attention_gb300 as gr
+    spec = workloads.WORKLOAD_BY_NAME[workloads.HEADLINE]
+    inp = workloads.make_inputs(spec)
+    torch.cuda.set_device(0)
+    gr.load()
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
+    shape = gr.Shape.of(inp)
+    widths = [int(w) for w in inp["widths"]]
+    ck, cv, cl = up(inp["ctx_k"]), up(inp["ctx_v"]), up(inp["ctx_len"])
+    bk, bv, bp = up(inp["beam_k"]), up(inp["beam_v"]), up(inp["beam_path"])
+    ok, ov, op = torch.empty_like(bk), torch.empty_like(bv), torch.empty_like(bp)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = {}
+    for step in range(len(widths)):
+        q = up(inp["q"][step])
+        R, W_s, Hq, D = spec.num_requests, widths[step], spec.num_q_heads, spec.head_dim
+        out = torch.empty(R * W_s * Hq * D, dtype=torch.int16, device="cuda")
+        lse = torch.empty(R * W_s * Hq, dtype=torch.float32, device="cuda")
+        flat = [W_s] * len(widths)
+        ws = torch.empty(max(16, gr.gr_decode_attn_workspace_size(shape, widths, step)), dtype=torch.uint8,
+                         device="cuda")
+        t_path, t_reorder, t_flat = [], [], []
+        for i in range(max(3, args.warmup) + args.steps):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            gr.gr_decode_attn(shape, q, ck, cv, cl, bk, bv, bp, widths, step, out, lse, ws)
+            e[1].record()
+            flush.zero_()
+            f = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            f[0].record()
+            gr.gr_beam_reorder(shape, bk, bv, bp, widths, step, ok, ov, op)
+            f[1].record()
+            gr.gr_decode_attn(shape, q, ck, cv, cl, ok, ov, op, flat, step, out, lse, ws)
+            f[2].record()
+            torch.cuda.synchronize()
+            if i >= max(3, args.warmup):
+                t_path.append(e[0].elapsed_time(e[1]) * 1000)
+                t_reorder.append(f[0].elapsed_time(f[1]) * 1000)
+                t_flat.append(f[1].elapsed_time(f[2]) * 1000)
+        res[step] = (float(np.mean(t_path)), float(np.mean(t_reorder)), float(np.mean(t_flat)))
+    line = {
+        "metric": "µs per decode step: attention through BeamPath vs reorder + attention on the reordered cache",
+        "value": float(np.mean([v[0] for v in res.values()])), "unit": "us/decode-step", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "higher_is_better": False, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(spec, inp),
+        "per_step": {str(k): {"beampath_us": round(v[0], 2), "reorder_us": round(v[1], 2),
+                              "attention_on_reordered_us": round(v[2], 2),
+                              "reorder_total_us": round(v[1] + v[2], 2)} for k, v in res.items()},
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.gpus != 1:
@@ -454,6 +514,8 @@ def main():
         return run_select_bench(args)
     if args.op == "trie_select":
         return run_trie_bench(args)
+    if args.op == "reorder":
+        return run_reorder_bench(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -358,6 +358,27 @@ int gr_trie_select(const gr_trie_select_shape *shape, const float *logits, const
                    int32_t *next_token, float *next_score, int32_t *next_node, void *workspace,
                    size_t workspace_bytes, gr_stream_t stream);
 
+/*
+ * The per-beam cache reordered along BeamPath, out of place (xGR review,
+ * "xAttention": the unshared cache is rearranged after each beam selection
+ * instead of being read through parent indices; the review's update formula
+ * is garbled, so this takes the plain reading):
+ *     out_k/out_v[r, t, b] = beam_k/beam_v[r, t, a_t(b)]  for t = 0..step, b < widths[step]
+ *     out_path[r, t, b]    = b for t >= 1 (0 at t = 0)
+ * with a_step = b, a_{t-1} = beam_path[r, t, a_t].  gr_decode_attn over
+ * (out_k, out_v, out_path) with every width set to widths[step] gives the
+ * same rows as over (beam_k, beam_v, beam_path) with `widths`.
+ *   out_k, out_v  device bf16 [R, S_max, W_max, Hkv, D], written at the rows above
+ *   out_path      device int32 [R, S_max, W_max], written at the entries above
+ * out_k/out_v must not be beam_k/beam_v (GR_ERR_BAD_SHAPE).  A parent outside
+ * [0, widths[t-1]) is not followed: the lower levels of that beam are not
+ * written and the device error word reports GR_ERR_BAD_BEAM_PATH.  Other
+ * errors as for gr_resolve_ancestors.
+ */
+int gr_beam_reorder(const gr_attn_shape *shape, const void *beam_k, const void *beam_v,
+                    const int32_t *beam_path, const int32_t *widths, int32_t step, void *out_k,
+                    void *out_v, int32_t *out_path, gr_stream_t stream);
+
 /* Static description of a gr_status code. */
 const char *gr_status_string(int status);
 
