@@ -173,3 +173,26 @@ def test_trie_select_workspace_and_bad_args(lib):
     assert call(stride=7) == -2
     assert call(logits=FAKE + 4) == -4
     assert call(ws_bytes=10) == -5
+
+
+def test_paged_and_reorder_reject_bad_args(lib):
+    w = (ctypes.c_int32 * 3)(4, 4, 4)
+    sh = ctypes.byref(_shape())
+
+    def paged(pages, table=FAKE):
+        return lib.gr_decode_attn_paged(sh, pages, FAKE, FAKE, FAKE, FAKE, table, FAKE, FAKE, FAKE, w, 2,
+                                        FAKE, FAKE, FAKE, 1 << 20, None)
+
+    assert paged(None) == -1
+    assert paged(ctypes.byref(gr.CtxPages(100, 4, 1))) == -2      # not a multiple of 128
+    assert paged(ctypes.byref(gr.CtxPages(128, 0, 1))) == -2      # no pages
+    assert paged(ctypes.byref(gr.CtxPages(128, 4, 0))) == -2      # empty block-table rows
+    assert paged(ctypes.byref(gr.CtxPages(128, 4, 1)), table=None) == -1
+    assert paged(ctypes.byref(gr.CtxPages(128, 4, 1)), table=FAKE + 4) == -4
+
+    def reorder(bk=FAKE, out_k=FAKE + 4096, out_path=FAKE + 8192):
+        return lib.gr_beam_reorder(sh, bk, FAKE + 1024, FAKE + 2048, w, 2, out_k, FAKE + 3072, out_path, None)
+
+    assert reorder(bk=None) == -1
+    assert reorder(out_path=FAKE + 8) == -4
+    assert reorder(out_k=FAKE) == -2                              # in place
