@@ -33,7 +33,7 @@ __all__ = [
     "gr_decode_attn_noalloc", "NOALLOC_SCRATCH_BYTES", "SelectShape", "gr_beam_select",
     "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
     "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size", "CtxPages",
-    "gr_decode_attn_paged", "gr_beam_reorder",
+    "gr_decode_attn_paged", "gr_beam_reorder", "gr_decode_attn_ragged",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
     "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
     "gr_trie_select_workspace_size", "gr_trie_select", "gr_decode_attn_paged", "gr_beam_reorder",
+    "gr_decode_attn_ragged",
 )
 
 # GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
@@ -179,6 +180,8 @@ def load() -> ctypes.CDLL:
     lib.gr_trie_select_workspace_size.restype = sz
     lib.gr_trie_select.argtypes = [tsp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz, vp]
     lib.gr_trie_select.restype = ctypes.c_int
+    lib.gr_decode_attn_ragged.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    lib.gr_decode_attn_ragged.restype = ctypes.c_int
     lib.gr_beam_reorder.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.gr_beam_reorder.restype = ctypes.c_int
     lib.gr_get_device_error.argtypes = []
@@ -383,6 +386,22 @@ def gr_trie_select(shape: TrieSelectShape, logits, beam_scores, beam_node, trie_
                                _ptr(next_score), _ptr(next_node), _ptr(workspace), int(workspace_bytes),
                                _stream_handle(stream))
     _check(rc, "gr_trie_select")
+
+
+def gr_decode_attn_ragged(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
+                          req_widths_host, req_widths, step: int, out, lse, workspace=None,
+                          workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """gr_decode_attn with a width per request: ``req_widths_host`` is a
+    [R][step+1] sequence, ``req_widths`` the device int32 [R, S_max] copy."""
+    flat = [int(w) for row in req_widths_host for w in row[:int(step) + 1]]
+    arr = (ctypes.c_int32 * max(1, len(flat)))(*flat)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().gr_decode_attn_ragged(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v), _ptr(ctx_len),
+                                      _ptr(beam_k), _ptr(beam_v), _ptr(beam_path), arr, _ptr(req_widths),
+                                      int(step), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                      _stream_handle(stream))
+    _check(rc, "gr_decode_attn_ragged")
 
 
 def gr_beam_reorder(shape: Shape, beam_k, beam_v, beam_path, widths: Sequence[int], step: int,

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) beam_merge_kernel(const Merg
     const long long rb = item / g.Hkv;
     const int b = (int)(rb % g.W_s);
     const int r = (int)(rb / g.W_s);
+    if (b >= width_of(g, r, g.step)) return;   // a row past its request's width (per-request widths)
 
     // ancestor walk: a_s = b, a_{t-1} = BeamPath[r, t, a_t]
     int ok = 1;
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) beam_merge_kernel(const Merg
         s_chain[warp][g.step] = slot;
         for (int t = g.step; t >= 1; --t) {
             const int p = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot);
-            if (p < 0 || p >= g.widths[t - 1]) { ok = 0; break; }
+            if (p < 0 || p >= width_of(g, r, t - 1)) { ok = 0; break; }
             slot = p;
             s_chain[warp][t - 1] = slot;
         }

@@ -227,7 +227,7 @@ __device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, 
             s_x[t * 2 * kBM + br[k].ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
             s_slot[t * 2 * kBM + br[k].ridx] = slot[k];
             if (t > 0) {
-                if (par[k] < 0 || par[k] >= g.widths[t - 1]) {
+                if (par[k] < 0 || par[k] >= width_of(g, r, t - 1)) {
                     bad[k] = 1;   // a parent out of range: nothing past it is read
                     on[k] = false;
                 } else {
@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool t1_active = (tile0 + 1) < p.tiles;
     const int rows_per_tile = p.bpt * g.G;
 
+    // with per-request widths, a CTA whose tiles lie past its request's width has no rows
+    if (g.req_widths && tile0 * p.bpt >= width_of(g, r, g.step)) return;
     int len = p.a.ctx_len[r];
     len = len < 0 ? 0 : (len > g.Lc_max ? g.Lc_max : len);
     const int kbeg = sp * p.a.sp.split_len;
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int m_local = b + 64 * k;
                         const int beam = (tile0 + t) * p.bpt + m_local / g.G;
                         BeamRow br[1];
-                        br[0].valid = (m_local < rows_per_tile) && (beam < g.W_s);
+                        br[0].valid = (m_local < rows_per_tile) && (beam < width_of(g, r, g.step));
                         br[0].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
                         br[0].beam = beam;
                         br[0].ridx = t * kBM + m_local;
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // this thread's row: beam b, query head kvh*G + m_local%G
         auto row_beam = [&]() { return (tile0 + t) * p.bpt + m_local / g.G; };
-        auto row_valid = [&]() { return (m_local < rows_per_tile) && (row_beam() < g.W_s); };
+        auto row_valid = [&]() { return (m_local < rows_per_tile) && (row_beam() < width_of(g, r, g.step)); };
         auto row_index = [&]() {
             return ((long long)r * g.W_s + row_beam()) * g.Hq + kvh * g.G + m_local % g.G;
         };

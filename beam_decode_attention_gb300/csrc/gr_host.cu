@@ -248,10 +248,15 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
                const int32_t *beam_path, const int32_t *widths, int32_t step, void *out, float *lse,
                void *workspace, size_t workspace_bytes, gr_stream_t stream,
                gr_event_t const *events, const gr_ctx_pages *pages = nullptr,
-               const int32_t *block_table = nullptr) {
+               const int32_t *block_table = nullptr, const int32_t *req_widths = nullptr) {
     Geometry g;
     int rc = make_geometry(shape, widths, step, &g);
     if (rc != GR_OK) return rc;
+    if (req_widths) {
+        if (misaligned(req_widths)) return GR_ERR_MISALIGNED;
+        if (chosen_path() == Path::kSimt) return GR_ERR_UNSUPPORTED;   // the cross-check path: shared widths only
+        g.req_widths = req_widths;
+    }
     if (pages) {
         if (pages->page_size < 128 || pages->page_size % 128 != 0 || pages->num_pages < 1 ||
             pages->pages_per_request < 1 ||
@@ -349,6 +354,28 @@ int gr_decode_attn_paged(const gr_attn_shape *shape, const gr_ctx_pages *pages, 
     if (!pages) return GR_ERR_NULL_ARG;
     return run_decode(shape, q, ctx_k_pool, ctx_v_pool, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
                       lse, workspace, workspace_bytes, stream, nullptr, pages, block_table);
+}
+
+int gr_decode_attn_ragged(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+                          const int32_t *ctx_len, const void *beam_k, const void *beam_v,
+                          const int32_t *beam_path, const int32_t *req_widths_host,
+                          const int32_t *req_widths, int32_t step, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, gr_stream_t stream) {
+    if (!shape || !req_widths_host || !req_widths) return GR_ERR_NULL_ARG;
+    if (shape->num_requests < 1 || step < 0 || step >= shape->step_capacity || step >= kMaxSteps)
+        return GR_ERR_BAD_SHAPE;
+    // the layout (and the plan) takes each step's largest width
+    int32_t wmax[kMaxSteps];
+    for (int t = 0; t <= step; ++t) {
+        wmax[t] = 0;
+        for (int r = 0; r < shape->num_requests; ++r) {
+            const int32_t w = req_widths_host[(long long)r * (step + 1) + t];
+            if (w < 1 || w > shape->beam_capacity) return GR_ERR_BAD_SHAPE;
+            wmax[t] = w > wmax[t] ? w : wmax[t];
+        }
+    }
+    return run_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, wmax, step, out, lse,
+                      workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, req_widths);
 }
 
 int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *ctx_k,

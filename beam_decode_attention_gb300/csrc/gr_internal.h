@@ -26,8 +26,17 @@ struct Geometry {
     int step, W_s;
     float scale;        // softmax scale applied to q.k (natural-log units)
     float scale_log2;   // softmax scale * log2(e)
-    int widths[kMaxSteps];
+    int widths[kMaxSteps];   // per step; with per-request widths, the largest over requests
+    // per-request widths (device int32 [R, S_max]; null: every request has
+    // widths[t]): rows b >= width(r, step) are not computed, and parents are
+    // checked against width(r, t - 1)
+    const int32_t *req_widths;
 };
+
+// the active width of request r at step t
+__host__ __device__ inline int width_of(const Geometry &g, int r, int t) {
+    return g.req_widths ? g.req_widths[(long long)r * g.S_max + t] : g.widths[t];
+}
 
 // Context-stage split of the key axis: split sp covers context positions
 // [sp * split_len, (sp + 1) * split_len) clipped to ctx_len[r].

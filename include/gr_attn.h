@@ -140,6 +140,27 @@ int gr_decode_attn_paged(const gr_attn_shape *shape, const gr_ctx_pages *pages, 
                          float *lse, void *workspace, size_t workspace_bytes, gr_stream_t stream);
 
 /*
+ * gr_decode_attn with a width per request (SID-GR README, section 10
+ * "TODO and Roadmap": per-request beam widths in one batch).  Request r has
+ * width W[r][t] at step t:
+ *   req_widths_host  HOST int32 [R][step+1]  (row stride step+1)
+ *   req_widths       device int32 [R, S_max]  the same values (read by the kernels)
+ * The tensors keep the shared layout with each step's largest width
+ * Wpad_t = max_r W[r][t]: q/out [R, Wpad_s, Hq, D], lse [R, Wpad_s, Hq].
+ * Rows b < W[r][step] are computed; rows past a request's width hold
+ * unspecified values.  Parents are checked against W[r][t-1].  The
+ * workspace is gr_decode_attn_workspace_size() with widths Wpad.  Errors as
+ * for gr_decode_attn; the CUDA-core cross-check path
+ * (GR_ATTN_FORCE_PATH=simt) returns GR_ERR_UNSUPPORTED.
+ */
+int gr_decode_attn_ragged(const gr_attn_shape *shape, const void *q, const void *ctx_k,
+                          const void *ctx_v, const int32_t *ctx_len, const void *beam_k,
+                          const void *beam_v, const int32_t *beam_path,
+                          const int32_t *req_widths_host, const int32_t *req_widths, int32_t step,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          gr_stream_t stream);
+
+/*
  * Size of the static device scratch gr_decode_attn_noalloc uses: 64 MiB.
  */
 #define GR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)

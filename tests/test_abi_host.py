@@ -196,3 +196,19 @@ def test_paged_and_reorder_reject_bad_args(lib):
     assert reorder(bk=None) == -1
     assert reorder(out_path=FAKE + 8) == -4
     assert reorder(out_k=FAKE) == -2                              # in place
+
+
+def test_ragged_rejects_bad_args(lib):
+    sh = ctypes.byref(_shape())
+
+    def ragged(host_w, dev_w=FAKE, step=2):
+        arr = None if host_w is None else (ctypes.c_int32 * len(host_w))(*host_w)
+        return lib.gr_decode_attn_ragged(sh, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, arr, dev_w, step,
+                                         FAKE, FAKE, FAKE, 1 << 20, None)
+
+    assert ragged(None) == -1
+    assert ragged([4, 4, 4, 2, 2, 2], dev_w=None) == -1
+    assert ragged([4, 4, 4, 2, 0, 2]) == -2                       # a width below 1
+    assert ragged([4, 4, 9, 2, 2, 2]) == -2                       # a width above beam_capacity
+    assert ragged([4, 4, 4, 2, 2, 2], step=3) == -2               # step past step_capacity
+    assert ragged([4, 4, 4, 2, 2, 2], dev_w=FAKE + 2) == -4       # misaligned device widths
