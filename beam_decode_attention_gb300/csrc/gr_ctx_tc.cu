@@ -149,6 +149,19 @@ __device__ __forceinline__ void kv_coords(const CtxArgs &a, int r, int key, int 
     }
 }
 
+// dlo += lo(a) * lo(b) and dhi += hi(a) * hi(b) for two packed bf16 pairs, in
+// fp32: the mixed-precision FMA takes the bf16 halves directly (bf16 -> fp32
+// is exact, so this equals fmaf on the widened values) with no unpacking.
+__device__ __forceinline__ void fma_bf16x2(float &dlo, float &dhi, uint32_t a, uint32_t b) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+        : "+f"(dlo), "+f"(dhi)
+        : "r"(a), "r"(b));
+}
+
 // One query row of the per-beam stage: its chain is walked by beam_prologue.
 struct BeamRow {
     bool valid;      // a row of this call (inside the tile and the step's width)
@@ -215,14 +228,10 @@ __device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, 
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint4 qv = q_chunk(k, ch);
                 const uint4 kc = kv[k][ch];
-                d0 = fmaf(__uint_as_float(qv.x << 16), __uint_as_float(kc.x << 16), d0);
-                d1 = fmaf(__uint_as_float(qv.x & 0xffff0000u), __uint_as_float(kc.x & 0xffff0000u), d1);
-                d2 = fmaf(__uint_as_float(qv.y << 16), __uint_as_float(kc.y << 16), d2);
-                d3 = fmaf(__uint_as_float(qv.y & 0xffff0000u), __uint_as_float(kc.y & 0xffff0000u), d3);
-                d0 = fmaf(__uint_as_float(qv.z << 16), __uint_as_float(kc.z << 16), d0);
-                d1 = fmaf(__uint_as_float(qv.z & 0xffff0000u), __uint_as_float(kc.z & 0xffff0000u), d1);
-                d2 = fmaf(__uint_as_float(qv.w << 16), __uint_as_float(kc.w << 16), d2);
-                d3 = fmaf(__uint_as_float(qv.w & 0xffff0000u), __uint_as_float(kc.w & 0xffff0000u), d3);
+                fma_bf16x2(d0, d1, qv.x, kc.x);
+                fma_bf16x2(d2, d3, qv.y, kc.y);
+                fma_bf16x2(d0, d1, qv.z, kc.z);
+                fma_bf16x2(d2, d3, qv.w, kc.w);
             }
             s_x[t * 2 * kBM + br[k].ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
             s_slot[t * 2 * kBM + br[k].ridx] = slot[k];
