@@ -35,7 +35,11 @@ struct Geometry {
 
 // the active width of request r at step t
 __host__ __device__ inline int width_of(const Geometry &g, int r, int t) {
-    return g.req_widths ? g.req_widths[(long long)r * g.S_max + t] : g.widths[t];
+    // a per-request width never exceeds the step's padded width, so a device
+    // copy that disagrees with the host's cannot index past the tensors
+    if (!g.req_widths) return g.widths[t];
+    const int w = g.req_widths[(long long)r * g.S_max + t];
+    return w < g.widths[t] ? w : g.widths[t];
 }
 
 // Context-stage split of the key axis: split sp covers context positions

@@ -144,7 +144,8 @@ int gr_decode_attn_paged(const gr_attn_shape *shape, const gr_ctx_pages *pages, 
  * "TODO and Roadmap": per-request beam widths in one batch).  Request r has
  * width W[r][t] at step t:
  *   req_widths_host  HOST int32 [R][step+1]  (row stride step+1)
- *   req_widths       device int32 [R, S_max]  the same values (read by the kernels)
+ *   req_widths       device int32 [R, S_max]  the same values (read by the kernels;
+ *                    a value above the step's padded width Wpad_t is taken as Wpad_t)
  * The tensors keep the shared layout with each step's largest width
  * Wpad_t = max_r W[r][t]: q/out [R, Wpad_s, Hq, D], lse [R, Wpad_s, Hq].
  * Rows b < W[r][step] are computed; rows past a request's width hold
