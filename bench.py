@@ -55,7 +55,8 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["attention", "beam_select", "trie_select", "reorder"], default="attention")
+    p.add_argument("--op", choices=["attention", "beam_select", "trie_select", "reorder", "paged", "ragged"],
+                   default="attention")
     return p.parse_args()
 
 
@@ -505,6 +506,95 @@ def run_reorder_bench(args):
     return 0
 
 
+RAGGED_WIDTHS = (900, 600, 300, 128)   # the four headline requests' widths in the ragged layout bench
+
+
+def run_layout_bench(args):
+    """The context and width layouts on the headline geometry, each against
+    the dense call on the same data, L2 flushed before every call:
+      paged   ContextKV in 128-key pages of a shuffled pool through a block table;
+      ragged  per-request widths 900 / 600 / 300 / 128 in one batch, against the
+              dense call over the same tensors at the largest width.
+    TFLOP/s count the rows each call computes (the ragged call: the active rows)."""
+    import torch
+    import beam_decode_attention_gb300 as gr
+    spec = workloads.WORKLOAD_BY_NAME[workloads.HEADLINE]
+    torch.cuda.set_device(0)
+    gr.load()
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
+    if args.op == "ragged":
+        inp, W = workloads.make_ragged(spec, [[w] * spec.steps for w in RAGGED_WIDTHS])
+    else:
+        inp, W = workloads.make_inputs(spec), None
+    shape = gr.Shape.of(inp)
+    widths = [int(w) for w in inp["widths"]]
+    ck, cv, cl = up(inp["ctx_k"]), up(inp["ctx_v"]), up(inp["ctx_len"])
+    bk, bv, bp = up(inp["beam_k"]), up(inp["beam_v"]), up(inp["beam_path"])
+    if args.op == "paged":
+        kp, table, ppr, P = workloads.paged_pool(inp["ctx_k"], 128, 8, seed=1)
+        vp, _, _, _ = workloads.paged_pool(inp["ctx_v"], 128, 8, seed=1)
+        pages = gr.CtxPages(128, P, ppr)
+        kp_d, vp_d, tb_d = up(kp), up(vp), up(table)
+    else:
+        wdev = np.zeros((spec.num_requests, spec.steps), np.int32)
+        wdev[:, :] = W
+        wdev_d = up(wdev)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(0).L2_cache_size, dtype=torch.uint8, device="cuda")
+    R, Hq, D = spec.num_requests, spec.num_q_heads, spec.head_dim
+    lc = [int(x) for x in inp["ctx_len"]]
+    res = {}
+    for step in range(spec.steps):
+        q = up(inp["q"][step])
+        W_s = widths[step]
+        out = torch.empty(R * W_s * Hq * D, dtype=torch.int16, device="cuda")
+        lse = torch.empty(R * W_s * Hq, dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, gr.gr_decode_attn_workspace_size(shape, widths, step)), dtype=torch.uint8,
+                         device="cuda")
+
+        def dense():
+            gr.gr_decode_attn(shape, q, ck, cv, cl, bk, bv, bp, widths, step, out, lse, ws)
+
+        def layout():
+            if args.op == "paged":
+                gr.gr_decode_attn_paged(shape, pages, q, kp_d, vp_d, cl, tb_d, bk, bv, bp, widths, step, out, lse, ws)
+            else:
+                gr.gr_decode_attn_ragged(shape, q, ck, cv, cl, bk, bv, bp, W.tolist(), wdev_d, step, out, lse, ws)
+
+        t_dense, t_layout = [], []
+        for i in range(max(3, args.warmup) + args.steps):
+            for fn, acc in ((dense, t_dense), (layout, t_layout)):
+                flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record()
+                fn()
+                e[1].record()
+                torch.cuda.synchronize()
+                if i >= max(3, args.warmup):
+                    acc.append(e[0].elapsed_time(e[1]) * 1000)
+        rows = [W_s] * R if W is None else [int(W[r, step]) for r in range(R)]
+        flops = sum(4.0 * D * Hq * rows[r] * (lc[r] + step + 1) for r in range(R))
+        dense_flops = sum(4.0 * D * Hq * W_s * (lc[r] + step + 1) for r in range(R))
+        res[step] = (float(np.mean(t_layout)), float(np.mean(t_dense)), flops, dense_flops)
+    err = gr.gr_get_device_error()
+    value = float(np.mean([v[0] for v in res.values()]))
+    line = {
+        "metric": ("µs per decode step, " + ("paged ContextKV (128-key pages, shuffled pool)" if args.op == "paged"
+                                            else "per-request widths 900/600/300/128 in one batch")
+                   + " against the dense call"),
+        "value": round(value, 3), "unit": "us/decode-step", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_of(spec, inp), layout=args.op,
+                       **({"request_widths": list(RAGGED_WIDTHS)} if args.op == "ragged" else {"page_size": 128})),
+        "per_step": {str(k): {"layout_us": round(v[0], 2), "dense_us": round(v[1], 2),
+                              "layout_tflops": round(v[2] / v[0] * 1e-6, 1),
+                              "dense_tflops": round(v[3] / v[1] * 1e-6, 1)} for k, v in res.items()},
+        "dense_value": round(float(np.mean([v[1] for v in res.values()])), 3),
+        "device_error": err,
+    }
+    print(json.dumps(line))
+    return 0 if err == 0 else 1
+
+
 def main():
     args = parse_args()
     if args.gpus != 1:
@@ -516,6 +606,8 @@ def main():
         return run_trie_bench(args)
     if args.op == "reorder":
         return run_reorder_bench(args)
+    if args.op in ("paged", "ragged"):
+        return run_layout_bench(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

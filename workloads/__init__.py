@@ -204,6 +204,49 @@ def make_custom(R: int, Hq: int, Hkv: int, D: int, ctx_len: Sequence[int],
 # entries, the Qwen3 tokenizer's embedding rows; the pages measure a fixed
 # width of 900 with full-vocabulary log-probabilities.
 
+# --------------------------------------------------------------------------- layouts of the context and widths
+#
+# A paged ContextKV pool built from a dense [R, Hkv, Lc_max, D] context: the
+# pages of all requests in a shuffled order (Generator(PCG64(seed))) with
+# `extra_pages` spare pages, each [Hkv, page_size, D]; positions past Lc_max
+# hold NaN.  Returns the pool [P, Hkv, page_size, D], the block table
+# [R, pages_per_request] int32, pages_per_request and P.
+
+def paged_pool(ctx: np.ndarray, page_size: int, extra_pages: int, seed: int):
+    R, Hkv, Lc, D = ctx.shape
+    ppr = max(1, -(-Lc // page_size))
+    P = R * ppr + extra_pages
+    order = np.random.Generator(np.random.PCG64(seed)).permutation(P)
+    pool = np.full((P, Hkv, page_size, D), BF16_NAN, np.uint16)
+    table = np.empty((R, ppr), np.int32)
+    for r in range(R):
+        for i in range(ppr):
+            page = int(order[r * ppr + i])
+            table[r, i] = page
+            seg = ctx[r, :, i * page_size:(i + 1) * page_size]
+            pool[page, :, :seg.shape[1]] = seg
+    return pool, table, ppr, P
+
+
+# Per-request widths over a workload laid out at each step's largest width:
+# request r has width widths[r][t] at step t, and its BeamPath parents are
+# folded into its own previous width (parent mod W[r][t-1]).  Returns the
+# modified inputs and W int32 [R, S].
+
+def make_ragged(spec: WorkloadSpec, widths: Sequence[Sequence[int]], seed: Optional[int] = None):
+    W = np.asarray(widths, np.int32)
+    if W.shape != (spec.num_requests, spec.steps) or np.any(W < 1):
+        raise ValueError("widths must be [requests][steps] of positive widths")
+    if np.any(W.max(axis=0) != np.asarray(spec.widths)):
+        raise ValueError("each step's largest width must be the workload's width")
+    inp = make_inputs(spec, seed)
+    bp = inp["beam_path"]
+    for r in range(W.shape[0]):
+        for t in range(1, W.shape[1]):
+            bp[r, t, :spec.widths[t]] %= W[r, t - 1]
+    return inp, W
+
+
 SELECT_HEADLINE = dict(num_requests=4, width=900, vocab=151936, next_width=900)
 
 
