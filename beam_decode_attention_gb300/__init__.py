@@ -194,7 +194,10 @@ def load() -> ctypes.CDLL:
     return lib
 
 
-def _widths_arr(widths: Sequence[int]):
+def _widths_arr(widths: Sequence[int], step: int):
+    """The per-step widths as a C array; the library reads widths[0..step]."""
+    if int(step) >= 0 and len(widths) < int(step) + 1:
+        raise ValueError("widths needs an entry for every step 0..step")
     arr = (ctypes.c_int32 * max(1, len(widths)))(*[int(w) for w in widths])
     return arr
 
@@ -229,7 +232,7 @@ def gr_version() -> int:
 
 
 def gr_decode_attn_workspace_size(shape: Shape, widths: Sequence[int], step: int) -> int:
-    w = _widths_arr(widths)
+    w = _widths_arr(widths, step)
     return int(load().gr_decode_attn_workspace_size(ctypes.byref(shape), w, int(step)))
 
 
@@ -242,7 +245,7 @@ def gr_decode_attn(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_
     (bf16 tensors may be ``torch.bfloat16`` or ``int16`` bit patterns).
     Raises :class:`GRError` on a non-zero status.
     """
-    w = _widths_arr(widths)
+    w = _widths_arr(widths, step)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().gr_decode_attn(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
@@ -256,7 +259,7 @@ def gr_decode_attn_paged(shape: Shape, pages: CtxPages, q, ctx_k_pool, ctx_v_poo
                          beam_k, beam_v, beam_path, widths: Sequence[int], step: int, out, lse,
                          workspace=None, workspace_bytes: Optional[int] = None, stream=None) -> None:
     """gr_decode_attn over a paged ContextKV pool (see ``include/gr_attn.h``)."""
-    w = _widths_arr(widths)
+    w = _widths_arr(widths, step)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().gr_decode_attn_paged(ctypes.byref(shape), ctypes.byref(pages), _ptr(q), _ptr(ctx_k_pool),
@@ -271,7 +274,7 @@ def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v,
                          workspace_bytes: Optional[int] = None, stream=None) -> None:
     """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``)
     before the context kernel, after it, and after the last kernel."""
-    w = _widths_arr(widths)
+    w = _widths_arr(widths, step)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     for e in events:
@@ -294,14 +297,14 @@ def gr_decode_attn_noalloc(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_
     more scratch than that."""
     rc = load().gr_decode_attn_noalloc(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
                                        _ptr(ctx_len), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path),
-                                       _widths_arr(widths), int(step), _ptr(out), _ptr(lse),
+                                       _widths_arr(widths, step), int(step), _ptr(out), _ptr(lse),
                                        _stream_handle(stream))
     _check(rc, "gr_decode_attn_noalloc")
 
 
 def gr_decode_attn_plan(shape: Shape, widths: Sequence[int], step: int) -> dict:
     info = PlanInfo()
-    rc = load().gr_decode_attn_plan(ctypes.byref(shape), _widths_arr(widths), int(step),
+    rc = load().gr_decode_attn_plan(ctypes.byref(shape), _widths_arr(widths, step), int(step),
                                     ctypes.byref(info))
     _check(rc, "gr_decode_attn_plan")
     return info.as_dict()
@@ -309,14 +312,14 @@ def gr_decode_attn_plan(shape: Shape, widths: Sequence[int], step: int) -> dict:
 
 def gr_resolve_ancestors(shape: Shape, beam_path, widths: Sequence[int], step: int, anc,
                          stream=None) -> None:
-    rc = load().gr_resolve_ancestors(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths),
+    rc = load().gr_resolve_ancestors(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths, step),
                                      int(step), _ptr(anc), _stream_handle(stream))
     _check(rc, "gr_resolve_ancestors")
 
 
 def gr_validate_beam_path(shape: Shape, beam_path, widths: Sequence[int], step: int, ctx_len,
                           bad_count, stream=None) -> None:
-    rc = load().gr_validate_beam_path(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths),
+    rc = load().gr_validate_beam_path(ctypes.byref(shape), _ptr(beam_path), _widths_arr(widths, step),
                                       int(step), _ptr(ctx_len), _ptr(bad_count),
                                       _stream_handle(stream))
     _check(rc, "gr_validate_beam_path")
@@ -393,7 +396,10 @@ def gr_decode_attn_ragged(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v
                           workspace_bytes: Optional[int] = None, stream=None) -> None:
     """gr_decode_attn with a width per request: ``req_widths_host`` is a
     [R][step+1] sequence, ``req_widths`` the device int32 [R, S_max] copy."""
-    flat = [int(w) for row in req_widths_host for w in row[:int(step) + 1]]
+    rows = [list(row) for row in req_widths_host]
+    if len(rows) != shape.num_requests or any(len(row) < int(step) + 1 for row in rows):
+        raise ValueError("req_widths_host needs num_requests rows of at least step + 1 widths")
+    flat = [int(w) for row in rows for w in row[:int(step) + 1]]
     arr = (ctypes.c_int32 * max(1, len(flat)))(*flat)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -408,7 +414,7 @@ def gr_beam_reorder(shape: Shape, beam_k, beam_v, beam_path, widths: Sequence[in
                     out_k, out_v, out_path, stream=None) -> None:
     """The per-beam cache reordered along BeamPath (see ``include/gr_attn.h``)."""
     rc = load().gr_beam_reorder(ctypes.byref(shape), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path),
-                                _widths_arr(widths), int(step), _ptr(out_k), _ptr(out_v), _ptr(out_path),
+                                _widths_arr(widths, step), int(step), _ptr(out_k), _ptr(out_v), _ptr(out_path),
                                 _stream_handle(stream))
     _check(rc, "gr_beam_reorder")
 

@@ -212,3 +212,18 @@ def test_ragged_rejects_bad_args(lib):
     assert ragged([4, 4, 9, 2, 2, 2]) == -2                       # a width above beam_capacity
     assert ragged([4, 4, 4, 2, 2, 2], step=3) == -2               # step past step_capacity
     assert ragged([4, 4, 4, 2, 2, 2], dev_w=FAKE + 2) == -4       # misaligned device widths
+
+
+def test_ragged_binding_checks_host_widths(lib):
+    # the binding refuses host widths that do not cover every request and step
+    sh = _shape()
+    for bad in ([[4, 4, 4]], [[4, 4], [2, 2]]):
+        with pytest.raises(ValueError):
+            gr.gr_decode_attn_ragged(sh, None, None, None, None, None, None, None, bad, None, 2, None, None)
+
+
+def test_binding_checks_widths_cover_the_step(lib):
+    with pytest.raises(ValueError):
+        gr.gr_decode_attn_workspace_size(_shape(), [4, 4], 2)    # widths for steps 0 and 1 only
+    with pytest.raises(ValueError):
+        gr.gr_decode_attn_plan(_shape(), [4], 1)
