@@ -215,11 +215,17 @@ def test_ragged_rejects_bad_args(lib):
 
 
 def test_ragged_binding_checks_host_widths(lib):
-    # the binding refuses host widths that do not cover every request and step
+    # the binding refuses host widths that do not cover every request and step,
+    # and a device width array smaller than [R, S_max] int32
+    import torch
     sh = _shape()
     for bad in ([[4, 4, 4]], [[4, 4], [2, 2]]):
         with pytest.raises(ValueError):
             gr.gr_decode_attn_ragged(sh, None, None, None, None, None, None, None, bad, None, 2, None, None)
+    for dev in (torch.zeros(2 * 2, dtype=torch.int32), torch.zeros(2 * 3, dtype=torch.int16)):
+        with pytest.raises(ValueError):
+            gr.gr_decode_attn_ragged(sh, None, None, None, None, None, None, None, [[4, 4, 4], [2, 2, 2]], dev, 2,
+                                     None, None)
 
 
 def test_binding_checks_widths_cover_the_step(lib):
