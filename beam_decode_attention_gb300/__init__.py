@@ -400,10 +400,12 @@ def gr_decode_attn_ragged(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v
     if len(rows) != shape.num_requests or any(len(row) < int(step) + 1 for row in rows):
         raise ValueError("req_widths_host needs num_requests rows of at least step + 1 widths")
     if req_widths is not None and hasattr(req_widths, "numel"):
-        # the kernels index the device copy as int32 [R, S_max]
-        if (req_widths.numel() < shape.num_requests * shape.step_capacity
-                or req_widths.element_size() != 4):
-            raise ValueError("req_widths must be a device int32 tensor of num_requests * step_capacity entries")
+        # the kernels index the device copy as a dense int32 [R, S_max]
+        import torch
+        if (req_widths.dtype != torch.int32 or not req_widths.is_cuda or not req_widths.is_contiguous()
+                or req_widths.numel() < shape.num_requests * shape.step_capacity):
+            raise ValueError("req_widths must be a contiguous device int32 tensor of "
+                             "num_requests * step_capacity entries")
     flat = [int(w) for row in rows for w in row[:int(step) + 1]]
     arr = (ctypes.c_int32 * max(1, len(flat)))(*flat)
     if workspace_bytes is None:

@@ -50,9 +50,6 @@ constexpr int kTmemCols = 512;
 // bf16 ranges, so the running maximum may lag the true one by up to 16 (log2)
 constexpr float kSumLimit = 65536.0f;
 constexpr int kFusedMaxTokens = 8;          // chain tokens the fused epilogue holds (steps < 8)
-// of every 8 column pairs, how many take exp2 from the FMA-pipe cubic instead
-// of the MUFU unit; on GB300 (ex2 at 32 lanes/clock/SM) all-MUFU measured fastest
-constexpr int kPolyPairs = 0;
 
 // barrier slots
 constexpr int kBarKvFull = 0;               // [kStages]
@@ -678,9 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rescale.  Past it (rare after the first block, or inf/NaN) the
                 // block maximum is taken from the scores still in registers, O and
                 // l are rescaled in TMEM and the pass is redone once.  Packed
-                // scale-and-subtract, exp2 on the MUFU unit (or the FMA-pipe cubic
-                // for kPolyPairs of every 8 pairs), packed row sums, and bf16 pairs
-                // stored over the first 64 S columns as P for the PV MMA.
+                // scale-and-subtract, exp2 on the MUFU unit, packed row sums, and
+                // bf16 pairs stored over the first 64 S columns as P for the PV MMA.
                 float blk = 0.f;
 #pragma unroll 1
                 for (int pass = 0; pass < 2; ++pass) {
@@ -695,12 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float s0 = __uint_as_float(sv[col]), s1 = __uint_as_float(sv[col + 1]);
                             float x0, x1, p0, p1;
                             ptx::ffma2(x0, x1, s0, s1, c, c, neg_m, neg_m);
-                            if ((j & 7) < kPolyPairs) {
-                                ptx::ex2_poly2(x0, x1, p0, p1);
-                            } else {
-                                p0 = ptx::ex2(x0);
-                                p1 = ptx::ex2(x1);
-                            }
+                            p0 = ptx::ex2(x0);
+                            p1 = ptx::ex2(x1);
                             ptx::fadd2(sa[j & 1], sb[j & 1], sa[j & 1], sb[j & 1], p0, p1);
                             pk[j] = pack_bf16x2(p0, p1);
                         }

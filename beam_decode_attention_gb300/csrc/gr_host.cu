@@ -65,6 +65,12 @@ int device_info(DeviceInfo *out) {
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// true when the byte ranges [a, a + na) and [b, b + nb) share a byte
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
 int make_geometry(const gr_attn_shape *s, const int32_t *widths, int32_t step, Geometry *g) {
     if (!s || !widths) return GR_ERR_NULL_ARG;
     if (s->num_requests < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->ctx_capacity < 0 ||
@@ -243,13 +249,24 @@ size_t gr_decode_attn_workspace_size(const gr_attn_shape *shape, const int32_t *
 
 namespace {
 
-int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
-               const int32_t *ctx_len, const void *beam_k, const void *beam_v,
-               const int32_t *beam_path, const int32_t *widths, int32_t step, void *out, float *lse,
-               void *workspace, size_t workspace_bytes, gr_stream_t stream,
-               gr_event_t const *events, const gr_ctx_pages *pages = nullptr,
-               const int32_t *block_table = nullptr, const int32_t *req_widths = nullptr) {
+// Everything gr_decode_attn decides before it enqueues work: the geometry,
+// the split plan, the workspace layout and the device facts.
+struct DecodeCall {
     Geometry g;
+    SplitPlan sp;
+    Layout lay;
+    DeviceInfo dev;
+};
+
+// Every host-side check of a decode call except the workspace size, in the
+// order the entry points report them: shape and widths, paged and
+// per-request-width descriptors, NULL pointers, alignment, then the device.
+int prepare_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+                   const int32_t *ctx_len, const void *beam_k, const void *beam_v, const int32_t *beam_path,
+                   const int32_t *widths, int32_t step, const void *out, const float *lse, const void *workspace,
+                   const gr_ctx_pages *pages, const int32_t *block_table, const int32_t *req_widths,
+                   DecodeCall *dc) {
+    Geometry &g = dc->g;
     int rc = make_geometry(shape, widths, step, &g);
     if (rc != GR_OK) return rc;
     if (req_widths) {
@@ -272,11 +289,27 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         misaligned(beam_k) || misaligned(beam_v) || misaligned(beam_path) || misaligned(out) ||
         misaligned(lse) || misaligned(workspace))
         return GR_ERR_MISALIGNED;
-    DeviceInfo dev;
-    rc = device_info(&dev);
+    rc = device_info(&dc->dev);
     if (rc != GR_OK) return rc;
-    const SplitPlan sp = plan(g, dev.sm_count);
-    const Layout lay = workspace_layout(g, sp);
+    dc->sp = plan(g, dc->dev.sm_count);
+    dc->lay = workspace_layout(g, dc->sp);
+    return GR_OK;
+}
+
+int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+               const int32_t *ctx_len, const void *beam_k, const void *beam_v,
+               const int32_t *beam_path, const int32_t *widths, int32_t step, void *out, float *lse,
+               void *workspace, size_t workspace_bytes, gr_stream_t stream,
+               gr_event_t const *events, const gr_ctx_pages *pages = nullptr,
+               const int32_t *block_table = nullptr, const int32_t *req_widths = nullptr) {
+    DecodeCall dc;
+    int rc = prepare_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out, lse,
+                            workspace, pages, block_table, req_widths, &dc);
+    if (rc != GR_OK) return rc;
+    const Geometry &g = dc.g;
+    const SplitPlan &sp = dc.sp;
+    const Layout &lay = dc.lay;
+    const DeviceInfo &dev = dc.dev;
     if (lay.total > 0 && (!workspace || workspace_bytes < lay.total)) return GR_ERR_WORKSPACE_TOO_SMALL;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -335,6 +368,20 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
 }
 
 }  // namespace
+
+namespace gr {
+
+int decode_scratch_bytes(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+                         const int32_t *ctx_len, const void *beam_k, const void *beam_v, const int32_t *beam_path,
+                         const int32_t *widths, int32_t step, const void *out, const float *lse, size_t *need) {
+    DecodeCall dc;
+    const int rc = prepare_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
+                                  lse, nullptr, nullptr, nullptr, nullptr, &dc);
+    if (rc == GR_OK) *need = dc.lay.total;
+    return rc;
+}
+
+}  // namespace gr
 
 extern "C" {
 
@@ -530,7 +577,19 @@ int gr_beam_reorder(const gr_attn_shape *shape, const void *beam_k, const void *
     if (misaligned(beam_k) || misaligned(beam_v) || misaligned(beam_path) || misaligned(out_k) ||
         misaligned(out_v) || misaligned(out_path))
         return GR_ERR_MISALIGNED;
-    if (out_k == beam_k || out_v == beam_v) return GR_ERR_BAD_SHAPE;   // out of place only
+    // out of place only: no output may share a byte with an input, since
+    // other CTAs still read the inputs while the outputs are written
+    {
+        const size_t kv = (size_t)g.R * g.S_max * g.W_max * g.Hkv * g.D * 2;
+        const size_t path = (size_t)g.R * g.S_max * g.W_max * sizeof(int32_t);
+        const void *in[3] = {beam_k, beam_v, beam_path};
+        const size_t in_bytes[3] = {kv, kv, path};
+        const void *outs[3] = {out_k, out_v, out_path};
+        const size_t out_bytes[3] = {kv, kv, path};
+        for (int i = 0; i < 3; ++i)
+            for (int j = 0; j < 3; ++j)
+                if (overlaps(outs[i], out_bytes[i], in[j], in_bytes[j])) return GR_ERR_BAD_SHAPE;
+    }
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != GR_OK) return rc;

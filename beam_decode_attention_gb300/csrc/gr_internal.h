@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "gr_attn.h"
+
 namespace gr {
 
 // Decode steps a call may name (widths travel to the kernels by value).
@@ -81,6 +83,13 @@ struct MergeArgs {
     float *lse;
     int *err;
 };
+
+// gr_host.cu: every host-side check gr_decode_attn makes except the
+// workspace size, in the same order; on GR_OK *need is the workspace the
+// call's plan uses
+int decode_scratch_bytes(const gr_attn_shape *shape, const void *q, const void *ctx_k, const void *ctx_v,
+                         const int32_t *ctx_len, const void *beam_k, const void *beam_v, const int32_t *beam_path,
+                         const int32_t *widths, int32_t step, const void *out, const float *lse, size_t *need);
 
 // gr_beam_merge.cu
 cudaError_t launch_beam_merge(const MergeArgs &a, cudaStream_t s);

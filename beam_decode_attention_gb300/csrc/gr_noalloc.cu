@@ -4,13 +4,13 @@
 // gr_decode_attn asks its caller for a device workspace, where the
 // context-stage kernel keeps its per-split partial results (an fp32 output
 // and a log-sum-exp per row and split) until the merge kernel combines them.
-// Some callers have no way to provide one: code that runs where CUDA API
-// calls that allocate are not allowed (a host callback enqueued on a
-// stream), code inside an engine whose memory pool has already reserved the
-// device memory (an extra cudaMalloc fails or breaks its accounting), and
-// latency-critical paths that cannot pay for cudaMalloc's implicit device
-// synchronisation.  For them this file keeps that scratch in a fixed-size
-// array in the library's own device memory.
+// Some callers have no way to provide one: code inside an engine whose
+// memory pool has already reserved the device memory (an extra cudaMalloc
+// fails or breaks its accounting), and latency-critical paths that cannot
+// pay for cudaMalloc's implicit device synchronisation.  For them this file
+// keeps that scratch in a fixed-size array in the library's own device
+// memory.  (Code running inside a stream callback cannot use this entry
+// point either: CUDA forbids every CUDA call there, launches included.)
 //
 // The array is a file-scope __device__ variable, so every GPU that loads
 // this library holds GR_NOALLOC_SCRATCH_BYTES of device memory for it until
@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "gr_attn.h"
+#include "gr_internal.h"
 
 namespace {
 
@@ -59,15 +60,18 @@ extern "C" int gr_decode_attn_noalloc(const gr_attn_shape *shape, const void *q,
                                       const void *beam_v, const int32_t *beam_path,
                                       const int32_t *widths, int32_t step, void *out, float *lse,
                                       gr_stream_t stream) {
-    if (!shape || !widths) return GR_ERR_NULL_ARG;
-    // The plan for this call decides how much scratch it needs; a call that
-    // needs more than the static array holds is refused before anything is
-    // enqueued.  A bad shape makes the size query return 0, and
-    // gr_decode_attn below reports the precise error.
-    const size_t need = gr_decode_attn_workspace_size(shape, widths, step);
+    // Every check gr_decode_attn makes, in its order (shapes, pointers,
+    // alignment, the device), runs first, so both entry points report the
+    // same error for the same arguments.  Then the plan's scratch need is
+    // compared with the static array: a call that needs more is refused
+    // before anything is enqueued.
+    size_t need = 0;
+    int rc = gr::decode_scratch_bytes(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step,
+                                      out, lse, &need);
+    if (rc != GR_OK) return rc;
     if (need > (size_t)GR_NOALLOC_SCRATCH_BYTES) return GR_ERR_WORKSPACE_TOO_SMALL;
     void *scratch = nullptr;
-    const int rc = scratch_address(&scratch);
+    rc = scratch_address(&scratch);
     if (rc != GR_OK) return rc;
     // Every entry of the scratch that the kernels read is written earlier in
     // the same call, so the previous call's leftovers need no clearing.

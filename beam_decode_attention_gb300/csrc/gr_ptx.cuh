@@ -249,27 +249,5 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 2^x for a pair on the FMA pipe instead of the MUFU unit: n = round(x)
-// through the 1.5*2^23 rounding constant, f = x - n in [-1/2, 1/2], 2^f by a
-// cubic minimax fit (max relative error 7.5e-5, coefficients derived by
-// csrc/exp2_poly_fit.py), and n added to the exponent field.  x is clamped
-// to >= -125 so that the result stays a normal number (2^-125 stands in for
-// 0 there).
-__device__ __forceinline__ void ex2_poly2(float x0, float x1, float &y0, float &y1) {
-    constexpr float kRound = 12582912.0f;   // 1.5 * 2^23
-    constexpr float kC0 = 0.99992812f, kC1 = 0.69326097f, kC2 = 0.24261053f, kC3 = 0.055171315f;
-    x0 = fmaxf(x0, -125.0f);
-    x1 = fmaxf(x1, -125.0f);
-    float t0, t1, n0, n1, f0, f1, p0, p1;
-    fadd2(t0, t1, x0, x1, kRound, kRound);
-    fadd2(n0, n1, t0, t1, -kRound, -kRound);
-    ffma2(f0, f1, n0, n1, -1.0f, -1.0f, x0, x1);
-    ffma2(p0, p1, f0, f1, kC3, kC3, kC2, kC2);
-    ffma2(p0, p1, p0, p1, f0, f1, kC1, kC1);
-    ffma2(p0, p1, p0, p1, f0, f1, kC0, kC0);
-    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
-
 }  // namespace ptx
 }  // namespace gr

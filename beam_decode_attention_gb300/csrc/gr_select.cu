@@ -686,15 +686,23 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
             tv = (int32_t)(flat % (uint32_t)a.V);
             sc = key_float((uint32_t)(e >> 32));
             if (a.next_node) {
-                // the edge of the parent's node that carries the token
+                // the edge of the parent's node that carries the token; the node
+                // and its edge range are checked as the rows kernel checks them,
+                // and a search that lands past the range or on another token (a
+                // node whose tokens are not increasing) gives no child
                 const int n = a.beam_node[(long long)r * a.W + pb];
-                int lo = a.trie_offsets[n], hi = a.trie_offsets[n + 1];
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (a.trie_tokens[mid] < tv) lo = mid + 1;
-                    else hi = mid;
+                if (n >= 0 && n < a.num_nodes) {
+                    const int e0 = a.trie_offsets[n], e1 = a.trie_offsets[n + 1];
+                    if (e0 >= 0 && e1 <= a.num_edges && e0 <= e1) {
+                        int lo = e0, hi = e1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            if (a.trie_tokens[mid] < tv) lo = mid + 1;
+                            else hi = mid;
+                        }
+                        if (lo < e1 && a.trie_tokens[lo] == tv) nd = a.trie_children[lo];
+                    }
                 }
-                nd = a.trie_children[lo];
             }
         }
         a.next_parent[(long long)r * a.parent_stride + j] = pb;

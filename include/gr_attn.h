@@ -169,15 +169,17 @@ int gr_decode_attn_ragged(const gr_attn_shape *shape, const void *q, const void 
 /*
  * gr_decode_attn for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point; it exists for callers such as
- * code running in a host callback enqueued on a stream (where CUDA calls
- * that allocate are not allowed), code inside an engine whose memory pool
- * already holds the device memory (so another cudaMalloc fails or breaks its
- * accounting), and latency-critical paths that cannot pay for cudaMalloc's
- * implicit synchronisation.
+ * code inside an engine whose memory pool already holds the device memory
+ * (so another cudaMalloc fails or breaks its accounting), and
+ * latency-critical paths that cannot pay for cudaMalloc's implicit
+ * synchronisation.  (A stream callback cannot call it: CUDA allows no CUDA
+ * call there at all, kernel launches included.)
  *
  * Same arguments, results and errors as gr_decode_attn, without the
  * workspace: the partial results live in a static device array of
- * GR_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU that loads the
+ * GR_NOALLOC_SCRATCH_BYTES inside the library.  Every check gr_decode_attn
+ * makes runs first, in the same order, so both report the same error for
+ * the same arguments.  Every GPU that loads the
  * library holds that array until the process exits.  The caller still
  * passes every input and output buffer.  This entry point allocates and
  * frees nothing.

@@ -71,11 +71,30 @@ class DeviceWorkload:
         return anc.cpu().numpy()
 
 
+def bf16_half_ulp(x):
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|: the
+    largest error of rounding the exact value x to a bf16 output."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(np.maximum(e, -133.0) - 8.0), 0.0)
+
+
 def compare(out, lse, ref_out, ref_lse, tol_out=1e-2, tol_lse=1e-3):
-    """Max-abs errors; asserts the gate and returns a small report."""
+    """Asserts the parity gate and returns a small report.
+
+    out: |out - oracle| <= tol_out + half a bf16 ulp of the oracle value.
+    The output format itself cannot hold the exact result: at |out| >= 4 a
+    bf16 step is 2^-5, so even the exactly computed, correctly rounded
+    result can sit 0.0156 from the fp64 oracle.  The 1e-2 gate therefore
+    bounds the error the kernel adds beyond that rounding.  lse (fp32):
+    |lse - oracle| <= tol_lse.  The plain max-abs errors are reported too.
+    """
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse)), "non-finite output"
-    e_out = float(np.max(np.abs(out.astype(np.float64) - ref_out))) if out.size else 0.0
+    diff = np.abs(out.astype(np.float64) - ref_out)
+    e_out = float(np.max(diff)) if out.size else 0.0
+    excess = float(np.max(diff - bf16_half_ulp(ref_out))) if out.size else 0.0
     e_lse = float(np.max(np.abs(lse.astype(np.float64) - ref_lse))) if lse.size else 0.0
-    assert e_out <= tol_out, f"max |out - oracle| = {e_out:.3e} > {tol_out}"
+    assert excess <= tol_out, (f"max |out - oracle| beyond the bf16 output rounding = {excess:.3e} > {tol_out} "
+                               f"(max-abs {e_out:.3e})")
     assert e_lse <= tol_lse, f"max |lse - oracle| = {e_lse:.3e} > {tol_lse}"
-    return dict(max_abs_out=e_out, max_abs_lse=e_lse)
+    return dict(max_abs_out=e_out, max_out_beyond_rounding=excess, max_abs_lse=e_lse)

@@ -190,12 +190,22 @@ def test_paged_and_reorder_reject_bad_args(lib):
     assert paged(ctypes.byref(gr.CtxPages(128, 4, 1)), table=None) == -1
     assert paged(ctypes.byref(gr.CtxPages(128, 4, 1)), table=FAKE + 4) == -4
 
-    def reorder(bk=FAKE, out_k=FAKE + 4096, out_path=FAKE + 8192):
-        return lib.gr_beam_reorder(sh, bk, FAKE + 1024, FAKE + 2048, w, 2, out_k, FAKE + 3072, out_path, None)
+    # beam_k/beam_v of this shape are 2*3*8*8*128*2 = 98,304 bytes, beam_path 192 bytes:
+    # the fake buffers below sit 1 MiB apart, so only the ones a case moves overlap
+    MB = 1 << 20
+    bk0, bv0, bp0, ok0, ov0, op0 = (FAKE + i * MB for i in range(6))
+
+    def reorder(bk=bk0, out_k=ok0, out_v=ov0, out_path=op0):
+        return lib.gr_beam_reorder(sh, bk, bv0, bp0, w, 2, out_k, out_v, out_path, None)
 
     assert reorder(bk=None) == -1
-    assert reorder(out_path=FAKE + 8) == -4
-    assert reorder(out_k=FAKE) == -2                              # in place
+    assert reorder(out_path=op0 + 8) == -4
+    assert reorder(out_k=bk0) == -2                               # in place
+    assert reorder(out_path=bp0) == -2                            # the path in place
+    assert reorder(out_v=bk0 + 98304 - 16) == -2                  # overlaps the end of beam_k
+    assert reorder(out_k=bv0 - 98304 + 16) == -2                  # overlaps the start of beam_v
+    assert reorder(out_path=bk0 + 4096) == -2                     # inside beam_k
+    assert reorder(out_v=bk0 + 98304) not in (-1, -2, -4)         # adjacent, not overlapping: passes the checks
 
 
 def test_ragged_rejects_bad_args(lib):
@@ -222,7 +232,10 @@ def test_ragged_binding_checks_host_widths(lib):
     for bad in ([[4, 4, 4]], [[4, 4], [2, 2]]):
         with pytest.raises(ValueError):
             gr.gr_decode_attn_ragged(sh, None, None, None, None, None, None, None, bad, None, 2, None, None)
-    for dev in (torch.zeros(2 * 2, dtype=torch.int32), torch.zeros(2 * 3, dtype=torch.int16)):
+    for dev in (torch.zeros(2 * 2, dtype=torch.int32), torch.zeros(2 * 3, dtype=torch.int16),
+                torch.zeros(2 * 3, dtype=torch.float32), torch.zeros(2 * 3, dtype=torch.int32),
+                torch.zeros(2 * 6, dtype=torch.int32)[::2]):
+        # too small, int16, float32, on the host, not contiguous
         with pytest.raises(ValueError):
             gr.gr_decode_attn_ragged(sh, None, None, None, None, None, None, None, [[4, 4, 4], [2, 2, 2]], dev, 2,
                                      None, None)
@@ -233,3 +246,41 @@ def test_binding_checks_widths_cover_the_step(lib):
         gr.gr_decode_attn_workspace_size(_shape(), [4, 4], 2)    # widths for steps 0 and 1 only
     with pytest.raises(ValueError):
         gr.gr_decode_attn_plan(_shape(), [4], 1)
+
+
+def _noalloc(shape, widths=(4, 4, 4), step=2, **ptrs):
+    lib = gr.load()
+    p = dict(q=FAKE, ck=FAKE, cv=FAKE, cl=FAKE, bk=FAKE, bv=FAKE, bp=FAKE, out=FAKE, lse=FAKE)
+    p.update(ptrs)
+    w = (ctypes.c_int32 * len(widths))(*widths)
+    return lib.gr_decode_attn_noalloc(ctypes.byref(shape), p["q"], p["ck"], p["cv"], p["cl"], p["bk"],
+                                      p["bv"], p["bp"], w, step, p["out"], p["lse"], 0)
+
+
+def test_noalloc_reports_the_same_errors_in_the_same_order(lib):
+    """gr_decode_attn_noalloc runs gr_decode_attn's checks, in its order,
+    before it looks up its static scratch: shape, NULL and alignment errors
+    come back as gr_decode_attn reports them, and with every argument valid
+    the first failure is the device check (no GPU here), as for
+    gr_decode_attn."""
+    cases = [
+        (dict(), dict()),
+        (dict(), dict(q=None)),
+        (dict(), dict(lse=None)),
+        (dict(), dict(out=FAKE + 2)),
+        (dict(), dict(bp=FAKE + 4)),
+        (dict(), dict(q=None, out=FAKE + 2)),
+        (dict(head_dim=96), dict()),
+        (dict(head_dim=96), dict(q=None)),
+        (dict(num_q_heads=12), dict(q=None)),
+        (dict(step=5), dict()),
+    ]
+    for shape_kw, ptrs in cases:
+        step = shape_kw.pop("step", 2)
+        sh = _shape(**shape_kw)
+        want = _call(sh, step=step, **dict(ptrs, ws=FAKE))
+        got = _noalloc(sh, step=step, **ptrs)
+        assert got == want, (shape_kw, ptrs, got, want)
+    assert _noalloc(_shape(), q=None) == -1
+    assert _noalloc(_shape(), out=FAKE + 2) == -4
+    assert _noalloc(_shape(), widths=(4, 0, 4)) == -2

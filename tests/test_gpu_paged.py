@@ -1,5 +1,6 @@
 """gr_decode_attn_paged (ContextKV in pages of a shared pool, through a block
-table) against gr_decode_attn on the same data in the dense layout: the
+table) against the CPU oracle on the dense copy of the same context, within
+the parity gate; and against gr_decode_attn on the dense layout, where the
 context kernel reads the same values in the same order, so the outputs must
 be bit-identical, in the fused single-split path and the split path."""
 
@@ -8,6 +9,7 @@ import os
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -17,7 +19,9 @@ if not torch.cuda.is_available():   # pragma: no cover - CPU-only machines
     pytest.skip("needs a GPU", allow_module_level=True)
 
 import beam_decode_attention_gb300 as gr  # noqa: E402
-from gpu_util import DeviceWorkload, to_dev  # noqa: E402
+from gpu_util import DeviceWorkload, compare, to_dev  # noqa: E402
+
+ORC = oracle.Oracle()
 
 
 def paged_pool(ctx, page_size, extra_pages, seed):
@@ -62,6 +66,34 @@ def test_paged_matches_dense_bit_for_bit(page_size, splits):
             assert np.array_equal(lse.cpu().numpy().reshape(dense_lse.shape), dense_lse, equal_nan=True)
     finally:
         os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+
+
+@pytest.mark.parametrize("page_size,splits", [(128, 1), (256, 1), (128, 2), (256, 2), (128, 3), (256, 3)])
+def test_paged_meets_the_oracle(page_size, splits):
+    """Every row of every step against the fp64 oracle on the dense context;
+    one request has no context, one a context that ends inside a page."""
+    inp = workloads.make_custom(3, 16, 8, 128, [900, 0, 1000], [7, 60, 129], seed=7 * page_size + splits,
+                                lc_max=1000)
+    dev = DeviceWorkload(inp)
+    kp, table, ppr, P = paged_pool(inp["ctx_k"], page_size, 3, seed=page_size)
+    vp, _, _, _ = paged_pool(inp["ctx_v"], page_size, 3, seed=page_size)
+    pages = gr.CtxPages(page_size, P, ppr)
+    kp_d, vp_d, tb_d = to_dev(kp), to_dev(vp), to_dev(table)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    try:
+        for step in range(3):
+            out, lse = dev.outputs(step)
+            ws = torch.empty(max(16, gr.gr_decode_attn_workspace_size(dev.shape, dev.widths, step)),
+                             dtype=torch.uint8, device="cuda")
+            gr.gr_decode_attn_paged(dev.shape, pages, dev.q[step], kp_d, vp_d, dev.ctx_len, tb_d, dev.beam_k,
+                                    dev.beam_v, dev.beam_path, dev.widths, step, out, lse, ws)
+            torch.cuda.synchronize()
+            ref_out, ref_lse, _ = ORC.decode_attn(inp, step)
+            got = (out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+            compare(got.reshape(ref_out.shape), lse.cpu().numpy().reshape(ref_lse.shape), ref_out, ref_lse)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+    assert gr.gr_get_device_error() == 0
 
 
 def test_paged_rejects_bad_descriptors():

@@ -59,6 +59,17 @@ def test_small_workloads_every_row(name, step):
     assert np.array_equal(dev.ancestors(step), ref_anc)
 
 
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_headline_workload_every_row(step):
+    """The measured workload (4 requests, 2048 context keys, 900 beams) in the
+    plan and launch configuration the benchmark times: every row."""
+    inp, dev = workload(workloads.HEADLINE)
+    out, lse = dev.run(step, guard=64)
+    ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+    compare(out, lse, ref_out, ref_lse)
+    assert np.array_equal(dev.ancestors(step), ref_anc)
+
+
 @pytest.mark.parametrize("name", [w.name for w in workloads.WORKLOADS[2:]])
 @pytest.mark.parametrize("step", [0, 1, 2])
 def test_full_size_sampled_rows(name, step):
@@ -176,6 +187,43 @@ def test_tagged_beam_values():
         ref_out, ref_lse, _ = ORC.decode_attn(inp, step)
         assert float(np.max(np.abs(ref_out))) > 0.2
         compare(out, lse, ref_out, ref_lse)
+
+
+def test_tagged_values_at_the_headline_geometry_fused():
+    """The fused single-split epilogue at the headline geometry (Qwen3-0.6B
+    heads, G = 2, 64 beams per 128-row tile, 900 beams: 14 full tiles and an
+    8-row tail tile) with a strong signal.  Context V = 0 and each chain
+    token's V is a random +-1 code of (request, step, slot, kv head), so out
+    is the chain tokens' weights times their codes: a wrong ancestor, a
+    missing chain term or a row written to the wrong place gives an O(0.1-1)
+    error.  Queries x4 and chain keys x3 make the chain tokens carry a large
+    share of the weight even against 2048 context keys; ctx_len 0 and 1 give
+    chain-only rows.  Every row of every request at every step."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(4, 16, 8, 128, [2048, 0, 1, 2048], [900, 900, 900], seed=303, q_scale=4.0)
+    inp["ctx_v"][:, :, :, :] = np.where(inp["ctx_v"] == workloads.BF16_NAN, workloads.BF16_NAN, 0).astype(np.uint16)
+    bk = workloads.bf16_bits_to_f32(inp["beam_k"])
+    inp["beam_k"] = workloads.f32_to_bf16_bits(bk * 3.0)
+    rng = np.random.default_rng(304)
+    signs = rng.integers(0, 2, size=inp["beam_v"].shape)
+    inp["beam_v"] = np.where(signs == 1, 0x3F80, 0xBF80).astype(np.uint16)   # bf16 +1 / -1
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = "1"
+    try:
+        for step in range(3):
+            plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, step)
+            assert plan["fused_merge"] == 1 and plan["n_splits"] == 1
+            out, lse = dev.run(step, guard=64)
+            ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+            # the signal: chain-only rows are pure +-1 mixtures, and the
+            # context rows still carry large chain weights
+            assert float(np.max(np.abs(ref_out[1]))) > 0.9
+            assert float(np.mean(np.abs(ref_out[0]))) > 0.08
+            compare(out, lse, ref_out, ref_lse)
+            assert np.array_equal(dev.ancestors(step), ref_anc)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+    assert gr.gr_get_device_error() == 0
 
 
 @pytest.mark.parametrize("jump", [3.0, 40.0])

@@ -1,12 +1,15 @@
-"""gr_beam_reorder: decode attention over the reordered per-beam cache (the
-identity path, every level W_s wide) equals attention over the original
-cache through BeamPath, bit for bit, in the fused and the split path."""
+"""gr_beam_reorder: the reordered per-beam cache equals, byte for byte, the
+gather the CPU oracle's ancestor table defines; decode attention over it
+(the identity path, every level W_s wide) meets the oracle's gate on the
+original inputs, and equals attention over the original cache through
+BeamPath bit for bit, in the fused and the split path."""
 
 import os
 
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -16,7 +19,70 @@ if not torch.cuda.is_available():   # pragma: no cover - CPU-only machines
     pytest.skip("needs a GPU", allow_module_level=True)
 
 import beam_decode_attention_gb300 as gr  # noqa: E402
-from gpu_util import DeviceWorkload  # noqa: E402
+from gpu_util import DeviceWorkload, compare  # noqa: E402
+
+ORC = oracle.Oracle()
+
+
+def oracle_gather(inp, step):
+    """The reordered cache the oracle's ancestor table defines:
+    out[r, t, b] = beam_kv[r, t, a_t(b)] for t <= step, b < W_step, and the
+    identity path; every other entry keeps the poison it started with."""
+    anc = ORC.ancestors(inp, step)                      # [R, W_s, step+1]
+    W_s = int(inp["widths"][step])
+    ok = np.full_like(inp["beam_k"], 0x7FC0)
+    ov = np.full_like(inp["beam_v"], 0x7FC0)
+    op = np.full_like(inp["beam_path"], -1)
+    for r in range(inp["num_requests"]):
+        for t in range(step + 1):
+            ok[r, t, :W_s] = inp["beam_k"][r, t, anc[r, :, t]]
+            ov[r, t, :W_s] = inp["beam_v"][r, t, anc[r, :, t]]
+            op[r, t, :W_s] = np.arange(W_s) if t > 0 else 0
+    return ok, ov, op
+
+
+def _bits(t):
+    return t.cpu().numpy().view(np.uint16) if t.dtype == torch.int16 else t.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["qwen3_0.6b_r8_lc1024_w128", "qwen3_0.6b_r4_lc2048_w900"])
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_reordered_bytes_equal_the_oracle_gather(name, step):
+    inp = workloads.make_inputs(workloads.WORKLOAD_BY_NAME[name])
+    dev = DeviceWorkload(inp)
+    ok = torch.full_like(dev.beam_k, 0x7FC0)
+    ov = torch.full_like(dev.beam_v, 0x7FC0)
+    op = torch.full_like(dev.beam_path, -1)
+    gr.gr_beam_reorder(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, step, ok, ov, op)
+    torch.cuda.synchronize()
+    want_k, want_v, want_p = oracle_gather(inp, step)
+    assert np.array_equal(_bits(ok), want_k)
+    assert np.array_equal(_bits(ov), want_v)
+    assert np.array_equal(_bits(op), want_p)
+    assert gr.gr_get_device_error() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_attention_on_reordered_cache_meets_the_oracle(splits):
+    inp = workloads.make_custom(2, 16, 8, 128, [300, 1000], [5, 70, 133], seed=50 + splits)
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    try:
+        for step in (1, 2):
+            ok, ov, op = torch.empty_like(dev.beam_k), torch.empty_like(dev.beam_v), torch.empty_like(dev.beam_path)
+            gr.gr_beam_reorder(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, step, ok, ov, op)
+            flat = [dev.widths[step]] * len(dev.widths)
+            out, lse = dev.outputs(step)
+            ws = torch.empty(max(16, gr.gr_decode_attn_workspace_size(dev.shape, flat, step)),
+                             dtype=torch.uint8, device="cuda")
+            gr.gr_decode_attn(dev.shape, dev.q[step], dev.ctx_k, dev.ctx_v, dev.ctx_len, ok, ov, op, flat, step,
+                              out, lse, ws)
+            torch.cuda.synchronize()
+            ref_out, ref_lse, _ = ORC.decode_attn(inp, step)      # the original cache, through BeamPath
+            got = (out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+            compare(got.reshape(ref_out.shape), lse.cpu().numpy().reshape(ref_lse.shape), ref_out, ref_lse)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
 
 
 @pytest.mark.parametrize("splits", [1, 2])

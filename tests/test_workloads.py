@@ -49,3 +49,18 @@ def test_make_ragged_rejects_bad_widths():
         workloads.make_ragged(spec, [[0] * spec.steps] + good[1:])  # a width below 1
     with pytest.raises(ValueError):
         workloads.make_ragged(spec, [[max(1, w - 1) for w in spec.widths]] * spec.num_requests)   # no request at the padded width
+
+
+def test_parity_gate_rounding_allowance():
+    """The GPU parity gate allows half a bf16 ulp of the oracle value on top
+    of 1e-2: check that allowance against the bf16 rounding the workloads
+    use (it bounds every rounding error and is reached)."""
+    from gpu_util import bf16_half_ulp
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(200000) * s for s in (0.01, 1.0, 3.0, 100.0)]).astype(np.float32)
+    r = workloads.bf16_bits_to_f32(workloads.f32_to_bf16_bits(x)).astype(np.float64)
+    err = np.abs(r - x.astype(np.float64))
+    hu = bf16_half_ulp(x)
+    assert np.all(err <= hu)
+    assert np.max(err / hu) > 0.999
+    assert bf16_half_ulp(np.array([4.0]))[0] == 2.0 ** -6 and bf16_half_ulp(np.array([3.99]))[0] == 2.0 ** -7
