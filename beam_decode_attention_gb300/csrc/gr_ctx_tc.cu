@@ -61,7 +61,8 @@ constexpr int kBarODone = 2 * kStages + 5;  // [2]
 constexpr int kBarFin = 2 * kStages + 7;
 constexpr int kBarVTail = 2 * kStages + 8;     // the tail block's V rows past ctx_len are zeroed
 constexpr int kBarBeam = 2 * kStages + 9;      // chain slots and scores are in shared memory
-constexpr int kNumBars = 2 * kStages + 10;
+constexpr int kBarSlots = 2 * kStages + 10;    // every row's chain slots are in shared memory
+constexpr int kNumBars = 2 * kStages + 11;
 
 template <int D>
 struct Cfg {
@@ -159,97 +160,102 @@ __device__ __forceinline__ void fma_bf16x2(float &dlo, float &dhi, uint32_t a, u
         : "r"(a), "r"(b));
 }
 
-// One query row of the per-beam stage: its chain is walked by beam_prologue.
-struct BeamRow {
-    bool valid;      // a row of this call (inside the tile and the step's width)
-    long long row;   // global row index (r, beam, query head)
-    int beam;        // a_s: the row's beam at the current step
-    int ridx;        // the row's slot in the shared-memory tables
-    uint32_t q_smem; // the row's query in the swizzled Q tile
-    int swz;         // 128-byte swizzle phase of that row
-};
-
-// Per-beam (unshared) stage for NR rows at a time, run by the beam warps
-// while the context loop runs: walk BeamPath back from each row's beam
-// (a_s = b, a_{t-1} = BeamPath[r, t, a_t]), score each chain token against
-// the query (base-2 units), and keep slot and score in shared memory for the
-// epilogue.  The NR rows advance together, and a token's parent index and K
-// row are fetched together, so a token costs one memory round trip for all
-// NR rows; the chain's V rows are prefetched into L2 for the epilogue.
-template <int D, int NR>
-__device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, const BeamRow (&br)[NR],
-                                              bool q_in_smem, float *s_x, int *s_slot, int *s_bad) {
+// The per-beam (unshared) stage, part 1, run by each softmax thread for its
+// own row before its first context block: walk BeamPath back from the row's
+// beam (a_s = b, a_{t-1} = BeamPath[r, t, a_t]) and keep every level's slot
+// in shared memory.  A parent outside [0, W_{t-1}) is not followed: the row
+// is flagged and nothing past it is read.  All rows walk at once, so the
+// walk costs s dependent loads in all, while the first K/V blocks land.
+__device__ __forceinline__ void walk_chain(const CtxArgs &a, int r, int beam, int ridx, int *s_slot, int *s_bad) {
     const Geometry &g = a.g;
-    int slot[NR], bad[NR];
-    bool on[NR];
-#pragma unroll
-    for (int k = 0; k < NR; ++k) {
-        slot[k] = br[k].beam;
-        bad[k] = 0;
-        on[k] = br[k].valid;
-    }
-    // query chunk ch of row k: from the swizzled Q tile when it was loaded, else from global memory
-    auto q_chunk = [&](int k, int ch) -> uint4 {
-        uint4 v;
-        if (q_in_smem) {
-            const uint32_t addr =
-                br[k].q_smem + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ br[k].swz) * 16);
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(addr));
-        } else {
-            v = __ldg(reinterpret_cast<const uint4 *>(a.q + br[k].row * D) + ch);
+    int slot = beam, bad = 0;
+    s_slot[g.step * 2 * kBM + ridx] = slot;
+    for (int t = g.step; t >= 1; --t) {
+        const int par = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot);
+        if (par < 0 || par >= width_of(g, r, t - 1)) {
+            bad = 1;
+            break;
         }
-        return v;
-    };
-    for (int t = g.step; t >= 0; --t) {
-        int par[NR];
-        uint4 kv[NR][D / 8];
+        slot = par;
+        s_slot[(t - 1) * 2 * kBM + ridx] = slot;
+    }
+    s_bad[ridx] = bad;
+}
+
+// The per-beam stage, part 2, run by the two beam warps while the context
+// loop runs: the score of every chain token of every row (base-2 units),
+// kept in shared memory for the epilogue.  Work items are (beam, level)
+// pairs: a level's K row is loaded once for the G query heads of its beam,
+// two items are in flight per thread (the slots are known, so the loads are
+// independent), and the V row is prefetched into L2 for the epilogue.
+template <int D>
+__device__ __forceinline__ void score_chains(const CtxArgs &a, int r, int kvh, int tile0, bool t1_active, int bpt,
+                                             bool q_in_smem, uint32_t q_tiles, int tid, float *s_x,
+                                             const int *s_slot, const int *s_bad) {
+    constexpr int kTileBytes = (D / 64) * kBM * 128;
+    const Geometry &g = a.g;
+    const int nt = g.step + 1;
+    const int n_items = 2 * bpt * nt;
+    const int width = width_of(g, r, g.step);
+    for (int i0 = tid; i0 < n_items; i0 += 2 * 64) {
+        int ridx0[2], slot[2], t_of[2];
+        bool on[2];
+        uint4 kv[2][D / 8];
 #pragma unroll
-        for (int k = 0; k < NR; ++k) {
-            par[k] = 0;
-            if (!on[k]) continue;
-            if (t > 0) par[k] = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot[k]);
-            const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot[k]) * g.Hkv + kvh) * D;
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + 64 * u;
+            const int bs = i / nt, t = i % nt;
+            const int tile = bs / bpt, bl = bs % bpt;
+            ridx0[u] = tile * kBM + bl * g.G;
+            t_of[u] = t;
+            on[u] = i < n_items && (tile == 0 || t1_active) && (tile0 + tile) * bpt + bl < width &&
+                    s_bad[ridx0[u]] == 0;
+            slot[u] = on[u] ? s_slot[t * 2 * kBM + ridx0[u]] : 0;
+            if (!on[u]) continue;
+            const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot[u]) * g.Hkv + kvh) * D;
             const uint4 *kr = reinterpret_cast<const uint4 *>(a.beam_k + kv_off);
             asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off));
             if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off + 64));
 #pragma unroll
-            for (int ch = 0; ch < D / 8; ++ch) kv[k][ch] = __ldg(kr + ch);
+            for (int ch = 0; ch < D / 8; ++ch) kv[u][ch] = __ldg(kr + ch);
         }
 #pragma unroll
-        for (int k = 0; k < NR; ++k) {
-            if (!on[k]) continue;
-            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        for (int u = 0; u < 2; ++u) {
+            if (!on[u]) continue;
+            for (int h = 0; h < g.G; ++h) {
+                const int ridx = ridx0[u] + h;
+                const int tile = ridx / kBM, m_local = ridx % kBM;
+                const uint32_t q_row = q_tiles + (uint32_t)(tile * kTileBytes + m_local * 128);
+                const int swz = m_local & 7;
+                const long long row = ((long long)r * g.W_s + (tile0 + tile) * bpt + m_local / g.G) * g.Hq +
+                                      kvh * g.G + m_local % g.G;
+                float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < D / 8; ++ch) {
-                const uint4 qv = q_chunk(k, ch);
-                const uint4 kc = kv[k][ch];
-                fma_bf16x2(d0, d1, qv.x, kc.x);
-                fma_bf16x2(d2, d3, qv.y, kc.y);
-                fma_bf16x2(d0, d1, qv.z, kc.z);
-                fma_bf16x2(d2, d3, qv.w, kc.w);
-            }
-            s_x[t * 2 * kBM + br[k].ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
-            s_slot[t * 2 * kBM + br[k].ridx] = slot[k];
-            if (t > 0) {
-                if (par[k] < 0 || par[k] >= width_of(g, r, t - 1)) {
-                    bad[k] = 1;   // a parent out of range: nothing past it is read
-                    on[k] = false;
-                } else {
-                    slot[k] = par[k];
+                for (int ch = 0; ch < D / 8; ++ch) {
+                    uint4 qv;
+                    if (q_in_smem) {
+                        const uint32_t addr = q_row + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ swz) * 16);
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qv.x), "=r"(qv.y), "=r"(qv.z), "=r"(qv.w)
+                                     : "r"(addr));
+                    } else {
+                        qv = __ldg(reinterpret_cast<const uint4 *>(a.q + row * D) + ch);
+                    }
+                    const uint4 kc = kv[u][ch];
+                    fma_bf16x2(d0, d1, qv.x, kc.x);
+                    fma_bf16x2(d2, d3, qv.y, kc.y);
+                    fma_bf16x2(d0, d1, qv.z, kc.z);
+                    fma_bf16x2(d2, d3, qv.w, kc.w);
                 }
+                s_x[t_of[u] * 2 * kBM + ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
             }
         }
     }
-#pragma unroll
-    for (int k = 0; k < NR; ++k)
-        if (br[k].valid) s_bad[br[k].ridx] = bad[k];
 }
 
 // Merge for the row this thread owns (fused epilogue, single key split): the
 // context partial (O in TMEM, running max m in base-2 units, sum l) and the
-// chain tokens scored by beam_prologue are combined by log-sum-exp (the
+// chain tokens scored by score_chains are combined by log-sum-exp (the
 // merging stage); the fp32 LSE is written, and the final bf16 row goes into
 // `stage` (the tile's Q tile: row m_local, 128-byte swizzled as TMA lays it
 // out) for the tile's TMA store.  The chain's V rows were prefetched into L2
@@ -257,12 +263,18 @@ __device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, 
 // warp-collective, so every lane takes part in the O loads.  beam_ok is false
 // when the beam warps gave up (the call already reports a timeout): the row
 // is then written as NaN without reading the chain tables.
-template <int D>
+//
+// kPartial (split 0 of a call with several key splits): the merged row is
+// not final, since the other splits' context partials are still to come; it
+// is written as split 0's normalised fp32 partial and LSE instead, so that
+// the split merge (merge_splits) finds the chain folded into it.
+template <int D, bool kPartial>
 __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, long long row, bool row_ok,
                                               bool have_ctx, float m_ctx, float l_ctx, uint32_t tO,
                                               const float *s_x, const int *s_slot, const int *s_bad, int ridx,
                                               bool beam_ok, uint32_t stage, int m_local) {
     const Geometry &g = a.g;
+    float *po = kPartial ? a.part_o + row * D : nullptr;   // split 0's partial row
     auto stage_chunk = [&](int hh, int c) -> uint32_t {
         return stage + (uint32_t)(hh * (kBM * 128) + m_local * 128 + ((c ^ (m_local & 7)) << 4));
     };
@@ -293,10 +305,17 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
         if (!row_ok) continue;
         if (bad) {
             // NaN marks a row whose chain is broken
+            if (kPartial) {
+                const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(stage_chunk(hh, c)), "r"(0x7fc07fc0u)
-                             : "memory");
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<float4 *>(po + 64 * hh + 4 * c) = make_float4(nan, nan, nan, nan);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(stage_chunk(hh, c)), "r"(0x7fc07fc0u)
+                                 : "memory");
+            }
             continue;
         }
         const float wc = w_ctx * inv;
@@ -337,20 +356,124 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
                 }
             }
         }
+        if (kPartial) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage_chunk(hh, c)),
-                         "r"(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1])), "r"(pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3])),
-                         "r"(pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5])), "r"(pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]))
-                         : "memory");
+            for (int c = 0; c < 16; ++c)
+                *reinterpret_cast<float4 *>(po + 64 * hh + 4 * c) =
+                    make_float4(acc[4 * c + 0], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stage_chunk(hh, c)),
+                             "r"(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1])),
+                             "r"(pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3])),
+                             "r"(pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5])),
+                             "r"(pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]))
+                             : "memory");
+        }
     }
     if (!row_ok) return;
+    float *lse_out = kPartial ? a.part_lse + row : a.lse + row;
     if (bad) {
-        a.lse[row] = __int_as_float(0x7fc00000);
+        *lse_out = __int_as_float(0x7fc00000);
         if (beam_ok) raise_device_error(a.err, kDevErrBadParent);
         return;
     }
-    a.lse[row] = (m_tot + log2f(L)) * kLn2;
+    *lse_out = (m_tot + log2f(L)) * kLn2;
+}
+
+// The split merge, run by the 256 softmax threads of the last CTA of a
+// (request, kv head, tile pair) to finish its key split: every split has
+// written its normalised partial (O / l in fp32, LSE in natural-log units;
+// split 0's includes the chain tokens), and they are combined exactly by
+// log-sum-exp into the final bf16 row and fp32 LSE (the merging stage).
+// Phase 1, one thread per row slot: the row's LSEs (all loads in flight
+// together), their maximum M, the weights exp(lse_i - M) / sum and the final
+// LSE; the weights go to shared memory (s_w[split][slot]).  Phase 2, one warp
+// per row, lane l holding elements [l*V, l*V + V): eight rows at a time, so
+// that eight coalesced partial-row reads per split are in flight.  The
+// partials come from other CTAs, so they are read from L2 (ld.cg).  A NaN
+// partial (a broken chain) makes the row NaN.
+constexpr int kMaxMergeSplits = 16;   // splits the in-kernel merge takes
+
+template <int D>
+__device__ __forceinline__ void merge_splits(const CtxArgs &a, int r, int kvh, int tile0, bool t1_active, int bpt,
+                                             int warp8, int lane, float *s_w) {
+    constexpr int V = D / 32;
+    constexpr int kRows = 8;
+    const Geometry &g = a.g;
+    const long long n_rows = (long long)g.R * g.W_s * g.Hq;
+    const int rows_per_tile = bpt * g.G;
+    const int n = a.sp.n_splits;
+    // the global row of slot j (t = j / 128, m_local = j % 128), or -1
+    auto row_of = [&](int j) -> long long {
+        const int t = j / kBM, m_local = j % kBM;
+        if (t == 1 && !t1_active) return -1;
+        if (m_local >= rows_per_tile) return -1;
+        const int beam = (tile0 + t) * bpt + m_local / g.G;
+        if (beam >= width_of(g, r, g.step)) return -1;
+        return ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
+    };
+    {
+        const int j = warp8 * 32 + lane;
+        const long long row = row_of(j);
+        if (row >= 0) {
+            float l[kMaxMergeSplits];
+#pragma unroll
+            for (int sp = 0; sp < kMaxMergeSplits; ++sp)
+                l[sp] = sp < n ? __ldcg(a.part_lse + sp * n_rows + row) : -INFINITY;
+            float M = -INFINITY;
+#pragma unroll
+            for (int sp = 0; sp < kMaxMergeSplits; ++sp) M = fmaxf(M, l[sp]);
+            float wsum = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < kMaxMergeSplits; ++sp) {
+                l[sp] = exp2f((l[sp] - M) * kLog2e);   // an empty split (or one past n): 0
+                wsum += l[sp];
+            }
+            const float inv = 1.f / wsum;
+#pragma unroll
+            for (int sp = 0; sp < kMaxMergeSplits; ++sp)
+                if (sp < n) s_w[sp * 2 * kBM + j] = l[sp] * inv;
+            a.lse[row] = M + logf(wsum);
+        }
+    }
+    ptx::named_bar_sync(3, 8 * 32);
+    for (int j0 = warp8 * 32; j0 < warp8 * 32 + 32; j0 += kRows) {
+        long long row[kRows];
+        float o[kRows][V];
+#pragma unroll
+        for (int k = 0; k < kRows; ++k) {
+            row[k] = row_of(j0 + k);
+#pragma unroll
+            for (int e = 0; e < V; ++e) o[k][e] = 0.f;
+        }
+        for (int sp = 0; sp < n; ++sp) {
+            float po[kRows][V];
+#pragma unroll
+            for (int k = 0; k < kRows; ++k) {
+                if (row[k] < 0) continue;
+                const float *src = a.part_o + (sp * n_rows + row[k]) * D + lane * V;
+                if constexpr (V == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    po[k][0] = v.x; po[k][1] = v.y; po[k][2] = v.z; po[k][3] = v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    po[k][0] = v.x; po[k][1] = v.y;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kRows; ++k) {
+                if (row[k] < 0) continue;
+                const float w = s_w[sp * 2 * kBM + j0 + k];
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[k][e] = fmaf(w, po[k][e], o[k][e]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRows; ++k)
+            if (row[k] >= 0) store_bf16<V>(a.out + row[k] * D + lane * V, o[k]);
+    }
 }
 
 template <int D>
@@ -399,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarFin), 1);
         ptx::mbar_init(bar(kBarVTail), 1);
         ptx::mbar_init(bar(kBarBeam), 2);   // one arrival per beam warp
+        ptx::mbar_init(bar(kBarSlots), 8);  // one arrival per softmax warp
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -586,34 +710,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kBeamWarp) {
         // ------------------------------------------------------------ per-beam stage
-        // 64 threads, four rows each (rows b and b + 64 of each tile, one at a
-        // time: measured faster than two rows in flight, which load the SM's
-        // memory pipeline harder while the softmax warps use it), while the
-        // context loop runs; then one arrival per warp.
-        if (p.a.fused) {
-            bool okq = nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag);   // q is read from the Q tile
-            if (!okq) {
+        // 64 threads score the chain tokens while the context loop runs, once
+        // the softmax warps have walked every row's chain; then one arrival
+        // per warp.
+        if (p.a.fused || (p.a.split_merge && sp == 0)) {
+            bool ok_in = (nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag)) &&   // q is read from the Q tile
+                         wait_warp(bar(kBarSlots), 0, abort_flag);
+            if (!ok_in) {
                 fail();
             } else {
-                float *s_x = reinterpret_cast<float *>(smem + C::kBeamX);
-                int *s_slot = reinterpret_cast<int *>(smem + C::kBeamSlot);
-                int *s_bad = reinterpret_cast<int *>(smem + C::kBeamBad);
-                const int b = (warp - kBeamWarp) * 32 + lane;
-                for (int t = 0; t < 2; ++t) {
-                    if (t == 1 && !t1_active) break;
-                    for (int k = 0; k < 2; ++k) {
-                        const int m_local = b + 64 * k;
-                        const int beam = (tile0 + t) * p.bpt + m_local / g.G;
-                        BeamRow br[1];
-                        br[0].valid = (m_local < rows_per_tile) && (beam < width_of(g, r, g.step));
-                        br[0].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
-                        br[0].beam = beam;
-                        br[0].ridx = t * kBM + m_local;
-                        br[0].q_smem = sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u;
-                        br[0].swz = m_local & 7;
-                        beam_prologue<D, 1>(p.a, r, kvh, br, nb > 0, s_x, s_slot, s_bad);
-                    }
-                }
+                score_chains<D>(p.a, r, kvh, tile0, t1_active, p.bpt, nb > 0, sbase + C::kQOff,
+                                (warp - kBeamWarp) * 32 + lane, reinterpret_cast<float *>(smem + C::kBeamX),
+                                reinterpret_cast<const int *>(smem + C::kBeamSlot),
+                                reinterpret_cast<const int *>(smem + C::kBeamBad));
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarBeam));
@@ -640,6 +749,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto row_index = [&]() {
             return ((long long)r * g.W_s + row_beam()) * g.Hq + kvh * g.G + m_local % g.G;
         };
+        if (p.a.fused || (p.a.split_merge && sp == 0)) {
+            // the per-beam stage's chain walk, while the first K/V blocks land
+            if (tile_active && row_valid()) walk_chain(p.a, r, row_beam(), ridx, s_slot, s_bad);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarSlots));
+        }
         if (tile_active && nb > 0) {
             for (int i = 0; i < nb; ++i) {
                 const int valid = min(kBN, kend - (kbeg + i * kBN));
@@ -747,8 +862,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the final rows leave through this tile's Q tile (free: every S of
             // the tile has completed, the beam warps are done with q) by TMA
             const uint32_t stage = sbase + C::kQOff + t * C::kTileBytes;
-            beam_epilogue<D>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx, beam_ok, stage,
-                             m_local);
+            beam_epilogue<D, false>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx,
+                                    beam_ok, stage, m_local);
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(1 + t, 4 * 32);
             if (quarter == 0 && lane == 0) {
@@ -757,6 +872,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::bulk_commit();
                 ptx::bulk_wait_all();   // the rows are written before the CTA (and its shared memory) ends
             }
+        } else if (tile_active && p.a.split_merge && sp == 0) {
+            // split 0 of an in-kernel split merge: the chain is folded into its partial
+            const bool beam_ok = wait_warp(bar(kBarBeam), 0, abort_flag);
+            if (!beam_ok) fail();
+            beam_epilogue<D, true>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx,
+                                   beam_ok, 0u, m_local);
         } else if (tile_active) {
             const long long n_rows = (long long)g.R * g.W_s * g.Hq;
             float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
@@ -782,6 +903,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (row_ok)
                 p.a.part_lse[(long long)sp * n_rows + row] = (have && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
+        if (p.a.split_merge) {
+            // arrive on the (request, kv head, tile pair) counter once this CTA's
+            // partial rows are visible device-wide; the last split to arrive
+            // merges every split's partials into the final rows
+            volatile int *s_last = reinterpret_cast<volatile int *>(smem + C::kBarOff + kNumBars * 8 + 8);
+            __threadfence();
+            ptx::named_bar_sync(3, 8 * 32);
+            if (warp == 0 && lane == 0) {
+                const int item = (r * g.Hkv + kvh) * (int)gridDim.x + pair;
+                const int before = atomicAdd(p.a.counters + item, 1);
+                *s_last = (before == p.a.sp.n_splits - 1) ? 1 : 0;
+                __threadfence();
+            }
+            ptx::named_bar_sync(3, 8 * 32);
+            // the merge weights go to the Q tiles, free once every MMA is done
+            if (*s_last)
+                merge_splits<D>(p.a, r, kvh, tile0, t1_active, p.bpt, warp, lane,
+                                reinterpret_cast<float *>(smem + C::kQOff));
         }
     }
 
@@ -871,6 +1011,7 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
 
 int tc_beams_per_tile(int G) { return kBM / G; }
 int tc_fused_max_steps(int) { return kFusedMaxTokens; }
+int tc_merge_max_splits() { return kMaxMergeSplits; }
 
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s) {
     const int bpt = tc_beams_per_tile(a.g.G);

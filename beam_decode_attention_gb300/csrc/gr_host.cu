@@ -157,14 +157,39 @@ TcShape tc_shape(const Geometry &g) {
     return t;
 }
 
+// Whether a call with this many key splits keeps the split merge in the
+// context kernel (the chain must fit the fused epilogue's tables).
+bool tc_split_merge(const Geometry &g, int n_splits) {
+    return n_splits > 1 && n_splits <= tc_merge_max_splits() && g.step < tc_fused_max_steps(g.G);
+}
+
+// Split count for the tensor-core context stage, from a cost model of one
+// call (in microseconds, measured on GB300 with one CTA per SM): a CTA costs
+// kFixed (set-up, first S, epilogue) plus kPerBlock per 128-key block of its
+// split; CTAs run in waves of sm_count; several splits add the merge (in the
+// kernel while the chain fits its tables -- split 0's chain epilogue and the
+// last split's merge --, else a second kernel).  Fewer splits win ties.
 SplitPlan plan_tc(const Geometry &g, int sm_count) {
     SplitPlan p{0, 0};
     if (g.Lc_max == 0) return p;
     constexpr int kKeyBlock = 128;
+    constexpr double kFixed = 9.0, kPerBlock = 1.8, kMergeIn = 15.0, kMergeKernel = 17.0;
     const int blocks = (g.Lc_max + kKeyBlock - 1) / kKeyBlock;
     const long long ctas = (long long)tc_shape(g).pairs * g.R * g.Hkv;
     int n = forced_splits();
-    if (n == 0) n = (int)std::max<long long>(1, (sm_count + ctas - 1) / ctas);
+    if (n == 0) {
+        double best = 0.0;
+        for (int c = 1; c <= std::min(blocks, 32); ++c) {
+            const int per = (blocks + c - 1) / c;
+            const long long waves = (ctas * c + sm_count - 1) / std::max(1, sm_count);
+            const double t = (double)waves * (kFixed + kPerBlock * per) +
+                             (c > 1 ? (tc_split_merge(g, c) ? kMergeIn : kMergeKernel) : 0.0);
+            if (c == 1 || t < best - 1e-9) {
+                best = t;
+                n = c;
+            }
+        }
+    }
     n = std::min(n, blocks);
     const int per = (blocks + n - 1) / n;
     p.split_len = per * kKeyBlock;
@@ -185,7 +210,7 @@ long long context_ctas(const Geometry &g, const SplitPlan &sp) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t part_o, part_lse, total;
+    size_t part_o, part_lse, counters, counter_bytes, total;
 };
 
 // With a single key split (and a chain short enough for the kernel's
@@ -195,15 +220,24 @@ bool fused_merge(const Geometry &g, const SplitPlan &p) {
     return chosen_path() == Path::kTensorCore && p.n_splits == 1 && g.step < tc_fused_max_steps(g.G);
 }
 
+// With several key splits and such a chain, the split merge also stays in
+// the context kernel: partials and arrival counters in the workspace, one
+// kernel (plus the counters' reset).
+bool split_merge(const Geometry &g, const SplitPlan &p) {
+    return chosen_path() == Path::kTensorCore && tc_split_merge(g, p.n_splits);
+}
+
 Layout workspace_layout(const Geometry &g, const SplitPlan &p) {
-    Layout l{0, 0, 0};
+    Layout l{0, 0, 0, 0, 0};
     if (fused_merge(g, p)) return l;
     const size_t rows = (size_t)g.R * g.W_s * g.Hq;
     const size_t o_bytes = (size_t)p.n_splits * rows * g.D * sizeof(float);
     const size_t lse_bytes = (size_t)p.n_splits * rows * sizeof(float);
     l.part_o = 0;
     l.part_lse = align256(o_bytes);
-    l.total = p.n_splits ? align256(l.part_lse + lse_bytes) : 0;
+    l.counters = align256(l.part_lse + lse_bytes);
+    l.counter_bytes = split_merge(g, p) ? (size_t)tc_shape(g).pairs * g.R * g.Hkv * sizeof(int) : 0;
+    l.total = p.n_splits ? align256(l.counters + l.counter_bytes) : 0;
     return l;
 }
 
@@ -334,6 +368,8 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         c.part_lse = part_lse;
         c.err = dev.err_ptr;
         c.fused = fused_merge(g, sp) ? 1 : 0;
+        c.split_merge = split_merge(g, sp) ? 1 : 0;
+        c.counters = c.split_merge ? reinterpret_cast<int *>(ws + lay.counters) : nullptr;
         c.beam_k = static_cast<const uint16_t *>(beam_k);
         c.beam_v = static_cast<const uint16_t *>(beam_v);
         c.beam_path = beam_path;
@@ -345,11 +381,16 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
             c.pages_per_req = pages->pages_per_request;
             c.num_pages = pages->num_pages;
         }
+        if (c.split_merge) {
+            // the arrival counters start at zero in every call
+            rc = cuda_status(cudaMemsetAsync(c.counters, 0, lay.counter_bytes, s));
+            if (rc != GR_OK) return rc;
+        }
         rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
         if (rc != GR_OK) return rc;
     }
     if ((rc = mark(1)) != GR_OK) return rc;
-    if (fused_merge(g, sp)) return mark(2);
+    if (fused_merge(g, sp) || split_merge(g, sp)) return mark(2);
     MergeArgs m;
     m.g = g;
     m.n_splits = sp.n_splits;
@@ -449,7 +490,7 @@ int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32
     info->n_splits = sp.n_splits;
     info->split_len = sp.split_len;
     info->context_ctas = (int32_t)context_ctas(g, sp);
-    info->fused_merge = fused_merge(g, sp) ? 1 : 0;
+    info->fused_merge = (fused_merge(g, sp) || split_merge(g, sp)) ? 1 : 0;
     info->kernels = (sp.n_splits && !info->fused_merge) ? 2 : 1;
     return GR_OK;
 }

@@ -62,6 +62,14 @@ struct CtxArgs {
     // fused epilogue (one key split): the kernel also runs the per-beam
     // stage and the merge, and writes the final rows
     int fused;
+    // split merge in the kernel (several key splits, chain short enough for
+    // the fused epilogue): split 0 also runs the per-beam stage and folds the
+    // chain into its partial; every split writes its partial and arrives on
+    // its (request, kv head, tile pair) counter, and the last to arrive
+    // merges the partials into the final rows.  The counters are zero when
+    // the kernel starts.
+    int split_merge;
+    int *counters;    // int32 [R * Hkv * pairs]
     const uint16_t *beam_k, *beam_v;
     const int32_t *beam_path;
     uint16_t *out;
@@ -104,6 +112,7 @@ cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
 // gr_ctx_tc.cu  (tensor-core context stage)
 int tc_beams_per_tile(int G);
 int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
+int tc_merge_max_splits();      // the in-kernel split merge takes at most this many splits
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 
 // gr_reorder.cu  (per-beam cache reordered along BeamPath)

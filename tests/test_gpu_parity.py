@@ -169,6 +169,27 @@ def test_forced_splits(splits):
     _run_custom(inp, steps=[2], splits=splits)
 
 
+@pytest.mark.parametrize("splits", [2, 3, 4])
+def test_split_merge_in_kernel_several_tile_pairs(splits):
+    """Several key splits merged inside the context kernel (the last split of
+    each (request, kv head, tile pair) to finish merges): three tile pairs
+    per (request, kv head) with a ragged last pair, a request whose context
+    ends inside a split and one whose later splits are empty, every step in
+    a row (the arrival counters start from zero in every call)."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(3, 16, 8, 128, [1024, 130, 777], [16, 140, 300], seed=31 + splits)
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    try:
+        plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)
+        assert plan["n_splits"] == splits and plan["fused_merge"] == 1 and plan["kernels"] == 1
+        assert gr.gr_decode_attn_workspace_size(dev.shape, dev.widths, 2) > 0
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+    _run_custom(inp, splits=splits)
+    _run_custom(inp, splits=splits)      # the same workspace again
+
+
 def test_tagged_beam_values():
     """Context V = 0, each beam token's V is a one-hot code of (step, slot),
     queries sharpened x4: out names the chain tokens and their weights, so a
@@ -273,7 +294,8 @@ def test_bad_parent_is_reported_not_followed(splits):
     assert int(bad.item()) == 2
     os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
     try:
-        assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)["fused_merge"] == (1 if splits == 1 else 0)
+        plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)
+        assert plan["fused_merge"] == 1 and plan["kernels"] == 1 and plan["n_splits"] == splits
         out, lse = dev.run(2)
     finally:
         os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
@@ -362,8 +384,16 @@ def test_long_chain_beyond_fused_epilogue():
     dev = DeviceWorkload(inp)
     assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 8)["fused_merge"] == 0
     assert gr.gr_decode_attn_plan(dev.shape, dev.widths, 7)["fused_merge"] in (0, 1)
-    for step in (7, 8):
-        out, lse = dev.run(step, guard=16)
-        ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
-        compare(out, lse, ref_out, ref_lse)
-        assert np.array_equal(dev.ancestors(step), ref_anc)
+    for splits in (None, 2):
+        if splits is not None:
+            os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+        try:
+            plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, 8)
+            assert plan["kernels"] == 2 and plan["fused_merge"] == 0
+            for step in (7, 8):
+                out, lse = dev.run(step, guard=16)
+                ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+                compare(out, lse, ref_out, ref_lse)
+                assert np.array_equal(dev.ancestors(step), ref_anc)
+        finally:
+            os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
