@@ -61,8 +61,7 @@ constexpr int kBarODone = 2 * kStages + 5;  // [2]
 constexpr int kBarFin = 2 * kStages + 7;
 constexpr int kBarVTail = 2 * kStages + 8;     // the tail block's V rows past ctx_len are zeroed
 constexpr int kBarBeam = 2 * kStages + 9;      // chain slots and scores are in shared memory
-constexpr int kBarSlots = 2 * kStages + 10;    // every row's chain slots are in shared memory
-constexpr int kNumBars = 2 * kStages + 11;
+constexpr int kNumBars = 2 * kStages + 10;
 
 template <int D>
 struct Cfg {
@@ -160,102 +159,97 @@ __device__ __forceinline__ void fma_bf16x2(float &dlo, float &dhi, uint32_t a, u
         : "r"(a), "r"(b));
 }
 
-// The per-beam (unshared) stage, part 1, run by each softmax thread for its
-// own row before its first context block: walk BeamPath back from the row's
-// beam (a_s = b, a_{t-1} = BeamPath[r, t, a_t]) and keep every level's slot
-// in shared memory.  A parent outside [0, W_{t-1}) is not followed: the row
-// is flagged and nothing past it is read.  All rows walk at once, so the
-// walk costs s dependent loads in all, while the first K/V blocks land.
-__device__ __forceinline__ void walk_chain(const CtxArgs &a, int r, int beam, int ridx, int *s_slot, int *s_bad) {
-    const Geometry &g = a.g;
-    int slot = beam, bad = 0;
-    s_slot[g.step * 2 * kBM + ridx] = slot;
-    for (int t = g.step; t >= 1; --t) {
-        const int par = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot);
-        if (par < 0 || par >= width_of(g, r, t - 1)) {
-            bad = 1;
-            break;
-        }
-        slot = par;
-        s_slot[(t - 1) * 2 * kBM + ridx] = slot;
-    }
-    s_bad[ridx] = bad;
-}
+// One query row of the per-beam stage: its chain is walked by beam_prologue.
+struct BeamRow {
+    bool valid;      // a row of this call (inside the tile and the step's width)
+    long long row;   // global row index (r, beam, query head)
+    int beam;        // a_s: the row's beam at the current step
+    int ridx;        // the row's slot in the shared-memory tables
+    uint32_t q_smem; // the row's query in the swizzled Q tile
+    int swz;         // 128-byte swizzle phase of that row
+};
 
-// The per-beam stage, part 2, run by the two beam warps while the context
-// loop runs: the score of every chain token of every row (base-2 units),
-// kept in shared memory for the epilogue.  Work items are (beam, level)
-// pairs: a level's K row is loaded once for the G query heads of its beam,
-// two items are in flight per thread (the slots are known, so the loads are
-// independent), and the V row is prefetched into L2 for the epilogue.
-template <int D>
-__device__ __forceinline__ void score_chains(const CtxArgs &a, int r, int kvh, int tile0, bool t1_active, int bpt,
-                                             bool q_in_smem, uint32_t q_tiles, int tid, float *s_x,
-                                             const int *s_slot, const int *s_bad) {
-    constexpr int kTileBytes = (D / 64) * kBM * 128;
+// Per-beam (unshared) stage for NR rows at a time, run by the beam warps
+// while the context loop runs: walk BeamPath back from each row's beam
+// (a_s = b, a_{t-1} = BeamPath[r, t, a_t]), score each chain token against
+// the query (base-2 units), and keep slot and score in shared memory for the
+// epilogue.  The NR rows advance together, and a token's parent index and K
+// row are fetched together, so a token costs one memory round trip for all
+// NR rows; the chain's V rows are prefetched into L2 for the epilogue.
+template <int D, int NR>
+__device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, const BeamRow (&br)[NR],
+                                              bool q_in_smem, float *s_x, int *s_slot, int *s_bad) {
     const Geometry &g = a.g;
-    const int nt = g.step + 1;
-    const int n_items = 2 * bpt * nt;
-    const int width = width_of(g, r, g.step);
-    for (int i0 = tid; i0 < n_items; i0 += 2 * 64) {
-        int ridx0[2], slot[2], t_of[2];
-        bool on[2];
-        uint4 kv[2][D / 8];
+    int slot[NR], bad[NR];
+    bool on[NR];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int i = i0 + 64 * u;
-            const int bs = i / nt, t = i % nt;
-            const int tile = bs / bpt, bl = bs % bpt;
-            ridx0[u] = tile * kBM + bl * g.G;
-            t_of[u] = t;
-            on[u] = i < n_items && (tile == 0 || t1_active) && (tile0 + tile) * bpt + bl < width &&
-                    s_bad[ridx0[u]] == 0;
-            slot[u] = on[u] ? s_slot[t * 2 * kBM + ridx0[u]] : 0;
-            if (!on[u]) continue;
-            const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot[u]) * g.Hkv + kvh) * D;
+    for (int k = 0; k < NR; ++k) {
+        slot[k] = br[k].beam;
+        bad[k] = 0;
+        on[k] = br[k].valid;
+    }
+    // query chunk ch of row k: from the swizzled Q tile when it was loaded, else from global memory
+    auto q_chunk = [&](int k, int ch) -> uint4 {
+        uint4 v;
+        if (q_in_smem) {
+            const uint32_t addr =
+                br[k].q_smem + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ br[k].swz) * 16);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(addr));
+        } else {
+            v = __ldg(reinterpret_cast<const uint4 *>(a.q + br[k].row * D) + ch);
+        }
+        return v;
+    };
+    for (int t = g.step; t >= 0; --t) {
+        int par[NR];
+        uint4 kv[NR][D / 8];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            par[k] = 0;
+            if (!on[k]) continue;
+            if (t > 0) par[k] = __ldg(a.beam_path + ((long long)r * g.S_max + t) * g.W_max + slot[k]);
+            const long long kv_off = ((((long long)r * g.S_max + t) * g.W_max + slot[k]) * g.Hkv + kvh) * D;
             const uint4 *kr = reinterpret_cast<const uint4 *>(a.beam_k + kv_off);
             asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off));
             if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beam_v + kv_off + 64));
 #pragma unroll
-            for (int ch = 0; ch < D / 8; ++ch) kv[u][ch] = __ldg(kr + ch);
+            for (int ch = 0; ch < D / 8; ++ch) kv[k][ch] = __ldg(kr + ch);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (!on[u]) continue;
-            for (int h = 0; h < g.G; ++h) {
-                const int ridx = ridx0[u] + h;
-                const int tile = ridx / kBM, m_local = ridx % kBM;
-                const uint32_t q_row = q_tiles + (uint32_t)(tile * kTileBytes + m_local * 128);
-                const int swz = m_local & 7;
-                const long long row = ((long long)r * g.W_s + (tile0 + tile) * bpt + m_local / g.G) * g.Hq +
-                                      kvh * g.G + m_local % g.G;
-                float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        for (int k = 0; k < NR; ++k) {
+            if (!on[k]) continue;
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch) {
-                    uint4 qv;
-                    if (q_in_smem) {
-                        const uint32_t addr = q_row + (uint32_t)(ch >> 3) * (kBM * 128) + (uint32_t)(((ch & 7) ^ swz) * 16);
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(qv.x), "=r"(qv.y), "=r"(qv.z), "=r"(qv.w)
-                                     : "r"(addr));
-                    } else {
-                        qv = __ldg(reinterpret_cast<const uint4 *>(a.q + row * D) + ch);
-                    }
-                    const uint4 kc = kv[u][ch];
-                    fma_bf16x2(d0, d1, qv.x, kc.x);
-                    fma_bf16x2(d2, d3, qv.y, kc.y);
-                    fma_bf16x2(d0, d1, qv.z, kc.z);
-                    fma_bf16x2(d2, d3, qv.w, kc.w);
+            for (int ch = 0; ch < D / 8; ++ch) {
+                const uint4 qv = q_chunk(k, ch);
+                const uint4 kc = kv[k][ch];
+                fma_bf16x2(d0, d1, qv.x, kc.x);
+                fma_bf16x2(d2, d3, qv.y, kc.y);
+                fma_bf16x2(d0, d1, qv.z, kc.z);
+                fma_bf16x2(d2, d3, qv.w, kc.w);
+            }
+            s_x[t * 2 * kBM + br[k].ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
+            s_slot[t * 2 * kBM + br[k].ridx] = slot[k];
+            if (t > 0) {
+                if (par[k] < 0 || par[k] >= width_of(g, r, t - 1)) {
+                    bad[k] = 1;   // a parent out of range: nothing past it is read
+                    on[k] = false;
+                } else {
+                    slot[k] = par[k];
                 }
-                s_x[t_of[u] * 2 * kBM + ridx] = ((d0 + d1) + (d2 + d3)) * g.scale_log2;
             }
         }
     }
+#pragma unroll
+    for (int k = 0; k < NR; ++k)
+        if (br[k].valid) s_bad[br[k].ridx] = bad[k];
 }
 
 // Merge for the row this thread owns (fused epilogue, single key split): the
 // context partial (O in TMEM, running max m in base-2 units, sum l) and the
-// chain tokens scored by score_chains are combined by log-sum-exp (the
+// chain tokens scored by beam_prologue are combined by log-sum-exp (the
 // merging stage); the fp32 LSE is written, and the final bf16 row goes into
 // `stage` (the tile's Q tile: row m_local, 128-byte swizzled as TMA lays it
 // out) for the tile's TMA store.  The chain's V rows were prefetched into L2
@@ -522,7 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarFin), 1);
         ptx::mbar_init(bar(kBarVTail), 1);
         ptx::mbar_init(bar(kBarBeam), 2);   // one arrival per beam warp
-        ptx::mbar_init(bar(kBarSlots), 8);  // one arrival per softmax warp
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -710,19 +703,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kBeamWarp) {
         // ------------------------------------------------------------ per-beam stage
-        // 64 threads score the chain tokens while the context loop runs, once
-        // the softmax warps have walked every row's chain; then one arrival
-        // per warp.
+        // 64 threads, four rows each (rows b and b + 64 of each tile, one at a
+        // time: measured faster than two rows in flight, which load the SM's
+        // memory pipeline harder while the softmax warps use it), while the
+        // context loop runs; then one arrival per warp.
         if (p.a.fused || (p.a.split_merge && sp == 0)) {
-            bool ok_in = (nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag)) &&   // q is read from the Q tile
-                         wait_warp(bar(kBarSlots), 0, abort_flag);
-            if (!ok_in) {
+            bool okq = nb == 0 || wait_warp(bar(kBarQFull), 0, abort_flag);   // q is read from the Q tile
+            if (!okq) {
                 fail();
             } else {
-                score_chains<D>(p.a, r, kvh, tile0, t1_active, p.bpt, nb > 0, sbase + C::kQOff,
-                                (warp - kBeamWarp) * 32 + lane, reinterpret_cast<float *>(smem + C::kBeamX),
-                                reinterpret_cast<const int *>(smem + C::kBeamSlot),
-                                reinterpret_cast<const int *>(smem + C::kBeamBad));
+                float *s_x = reinterpret_cast<float *>(smem + C::kBeamX);
+                int *s_slot = reinterpret_cast<int *>(smem + C::kBeamSlot);
+                int *s_bad = reinterpret_cast<int *>(smem + C::kBeamBad);
+                const int b = (warp - kBeamWarp) * 32 + lane;
+                for (int t = 0; t < 2; ++t) {
+                    if (t == 1 && !t1_active) break;
+                    for (int k = 0; k < 2; ++k) {
+                        const int m_local = b + 64 * k;
+                        const int beam = (tile0 + t) * p.bpt + m_local / g.G;
+                        BeamRow br[1];
+                        br[0].valid = (m_local < rows_per_tile) && (beam < width_of(g, r, g.step));
+                        br[0].row = ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
+                        br[0].beam = beam;
+                        br[0].ridx = t * kBM + m_local;
+                        br[0].q_smem = sbase + C::kQOff + t * C::kTileBytes + (uint32_t)m_local * 128u;
+                        br[0].swz = m_local & 7;
+                        beam_prologue<D, 1>(p.a, r, kvh, br, nb > 0, s_x, s_slot, s_bad);
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarBeam));
@@ -749,12 +757,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto row_index = [&]() {
             return ((long long)r * g.W_s + row_beam()) * g.Hq + kvh * g.G + m_local % g.G;
         };
-        if (p.a.fused || (p.a.split_merge && sp == 0)) {
-            // the per-beam stage's chain walk, while the first K/V blocks land
-            if (tile_active && row_valid()) walk_chain(p.a, r, row_beam(), ridx, s_slot, s_bad);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(kBarSlots));
-        }
         if (tile_active && nb > 0) {
             for (int i = 0; i < nb; ++i) {
                 const int valid = min(kBN, kend - (kbeg + i * kBN));
