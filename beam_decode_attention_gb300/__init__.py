@@ -125,6 +125,7 @@ class PlanInfo(ctypes.Structure):
         ("context_ctas", ctypes.c_int32),
         ("kernels", ctypes.c_int32),
         ("fused_merge", ctypes.c_int32),
+        ("persistent", ctypes.c_int32),
     ]
 
     def as_dict(self):

@@ -109,11 +109,24 @@ int make_geometry(const gr_attn_shape *s, const int32_t *widths, int32_t step, G
 enum class Path { kTensorCore, kSimt };
 
 // GR_ATTN_FORCE_PATH=simt selects the CUDA-core context stage (a cross-check
-// of the tensor-core kernel in tests); the tensor-core stage is the default.
+// of the tensor-core kernels in tests); the tensor-core stage is the default.
 Path chosen_path() {
     const char *e = std::getenv("GR_ATTN_FORCE_PATH");
     if (e && std::strcmp(e, "simt") == 0) return Path::kSimt;
     return Path::kTensorCore;
+}
+
+// GR_ATTN_FORCE_PATH=pair keeps single-split calls on the tile-pair kernel,
+// GR_ATTN_FORCE_PATH=persistent puts them on the persistent one whatever the
+// cost model says (tests compare the two).
+bool pair_forced() {
+    const char *e = std::getenv("GR_ATTN_FORCE_PATH");
+    return e && std::strcmp(e, "pair") == 0;
+}
+
+bool persistent_forced() {
+    const char *e = std::getenv("GR_ATTN_FORCE_PATH");
+    return e && std::strcmp(e, "persistent") == 0;
 }
 
 int forced_splits() {
@@ -125,7 +138,7 @@ int forced_splits() {
 
 // Split plan for the CUDA-core context stage.
 SplitPlan plan_simt(const Geometry &g, int sm_count) {
-    SplitPlan p{0, 0};
+    SplitPlan p{0, 0, 0};
     if (g.Lc_max == 0) return p;
     constexpr int kKeyBlock = 32;
     const int blocks = (g.Lc_max + kKeyBlock - 1) / kKeyBlock;
@@ -142,9 +155,8 @@ SplitPlan plan_simt(const Geometry &g, int sm_count) {
     return p;
 }
 
-// Split plan for the tensor-core context stage: one CTA per (request, kv head,
-// pair of 128-row tiles, split); splits are added until the grid covers the
-// SMs once (one CTA fits per SM).
+// Tile geometry of the tensor-core kernels: beams per 128-row tile, tiles
+// per (request, kv head), and tile pairs (one tile-pair CTA per pair and split).
 struct TcShape {
     int bpt, tiles, pairs;
 };
@@ -163,25 +175,44 @@ bool tc_split_merge(const Geometry &g, int n_splits) {
     return n_splits > 1 && n_splits <= tc_merge_max_splits() && g.step < tc_fused_max_steps(g.G);
 }
 
-// Split count for the tensor-core context stage, from a cost model of one
-// call (in microseconds, measured on GB300 with one CTA per SM): a CTA costs
-// kFixed (set-up, first S, epilogue) plus kPerBlock per 128-key block of its
-// split; CTAs run in waves of sm_count; several splits add the merge (in the
-// kernel while the chain fits its tables -- split 0's chain epilogue and the
-// last split's merge --, else a second kernel).  Fewer splits win ties.
+// Whether a single-split call runs on the persistent kernel (chains short
+// enough for its epilogue tables, not forced onto the tile-pair kernel).
+bool tc_persistent(const Geometry &g, int n_splits) {
+    return n_splits == 1 && g.step < pk_max_steps() && !pair_forced();
+}
+
+// Kernel and split count for the tensor-core context stage, from a cost
+// model of one call (in microseconds, measured on GB300 with one CTA per
+// SM).  The tile-pair kernel: a CTA costs kFixed (set-up, first S,
+// epilogue) plus kPerBlock per 128-key block of its split, CTAs run in waves
+// of sm_count, and several splits add the merge, kMergeIn (in the kernel
+// while the chain fits its tables) or kMergeKernel (a second kernel).  The
+// persistent kernel (one split, 128-row tiles) is a candidate while every
+// tile has an SM of its own: one round of kPkFixed plus kPkPerBlock per
+// block.  Past one round the tile-pair kernel measured faster (each 128-row
+// tile then streams the whole context per block on its own SM, where a tile
+// pair shares it).  Fewer splits win ties.
 SplitPlan plan_tc(const Geometry &g, int sm_count) {
-    SplitPlan p{0, 0};
+    SplitPlan p{0, 0, 0};
     if (g.Lc_max == 0) return p;
     constexpr int kKeyBlock = 128;
     constexpr double kFixed = 9.0, kPerBlock = 1.8, kMergeIn = 15.0, kMergeKernel = 17.0;
+    constexpr double kPkFixed = 8.0, kPkPerBlock = 1.5;
     const int blocks = (g.Lc_max + kKeyBlock - 1) / kKeyBlock;
-    const long long ctas = (long long)tc_shape(g).pairs * g.R * g.Hkv;
+    const TcShape sh = tc_shape(g);
+    const long long ctas = (long long)sh.pairs * g.R * g.Hkv;
+    const long long items = (long long)sh.tiles * g.R * g.Hkv;
+    const int sms = std::max(1, sm_count);
     int n = forced_splits();
-    if (n == 0) {
+    bool pk = false;
+    if (n == 0 && persistent_forced() && tc_persistent(g, 1)) {
+        n = 1;
+        pk = true;
+    } else if (n == 0) {
         double best = 0.0;
         for (int c = 1; c <= std::min(blocks, 32); ++c) {
             const int per = (blocks + c - 1) / c;
-            const long long waves = (ctas * c + sm_count - 1) / std::max(1, sm_count);
+            const long long waves = (ctas * c + sms - 1) / sms;
             const double t = (double)waves * (kFixed + kPerBlock * per) +
                              (c > 1 ? (tc_split_merge(g, c) ? kMergeIn : kMergeKernel) : 0.0);
             if (c == 1 || t < best - 1e-9) {
@@ -189,22 +220,23 @@ SplitPlan plan_tc(const Geometry &g, int sm_count) {
                 n = c;
             }
         }
+        if (tc_persistent(g, 1) && items <= sms && kPkFixed + kPkPerBlock * blocks < best - 1e-9) {
+            n = 1;
+            pk = true;
+        }
+    } else if (n == 1 && tc_persistent(g, 1) && persistent_forced()) {
+        pk = true;
     }
     n = std::min(n, blocks);
     const int per = (blocks + n - 1) / n;
     p.split_len = per * kKeyBlock;
     p.n_splits = (g.Lc_max + p.split_len - 1) / p.split_len;
+    p.persistent = (pk && p.n_splits == 1) ? 1 : 0;
     return p;
 }
 
 SplitPlan plan(const Geometry &g, int sm_count) {
     return chosen_path() == Path::kSimt ? plan_simt(g, sm_count) : plan_tc(g, sm_count);
-}
-
-long long context_ctas(const Geometry &g, const SplitPlan &sp) {
-    if (sp.n_splits == 0) return 0;
-    if (chosen_path() == Path::kSimt) return (long long)((g.W_s * g.G + 15) / 16) * g.R * g.Hkv * sp.n_splits;
-    return (long long)tc_shape(g).pairs * g.R * g.Hkv * sp.n_splits;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -220,11 +252,23 @@ bool fused_merge(const Geometry &g, const SplitPlan &p) {
     return chosen_path() == Path::kTensorCore && p.n_splits == 1 && g.step < tc_fused_max_steps(g.G);
 }
 
+// The planner's choice of the persistent kernel.
+bool persistent(const Geometry &, const SplitPlan &p) {
+    return chosen_path() == Path::kTensorCore && p.persistent != 0;
+}
+
 // With several key splits and such a chain, the split merge also stays in
 // the context kernel: partials and arrival counters in the workspace, one
 // kernel (plus the counters' reset).
 bool split_merge(const Geometry &g, const SplitPlan &p) {
     return chosen_path() == Path::kTensorCore && tc_split_merge(g, p.n_splits);
+}
+
+long long context_ctas(const Geometry &g, const SplitPlan &sp, int sm_count) {
+    if (sp.n_splits == 0) return 0;
+    if (chosen_path() == Path::kSimt) return (long long)((g.W_s * g.G + 15) / 16) * g.R * g.Hkv * sp.n_splits;
+    if (persistent(g, sp)) return std::min<long long>((long long)tc_shape(g).tiles * g.R * g.Hkv, (long long)sm_count);
+    return (long long)tc_shape(g).pairs * g.R * g.Hkv * sp.n_splits;
 }
 
 Layout workspace_layout(const Geometry &g, const SplitPlan &p) {
@@ -386,7 +430,10 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
             rc = cuda_status(cudaMemsetAsync(c.counters, 0, lay.counter_bytes, s));
             if (rc != GR_OK) return rc;
         }
-        rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
+        if (persistent(g, sp))
+            rc = cuda_status(launch_ctx_pk(c, dev.sm_count, s));
+        else
+            rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
         if (rc != GR_OK) return rc;
     }
     if ((rc = mark(1)) != GR_OK) return rc;
@@ -489,9 +536,10 @@ int gr_decode_attn_plan(const gr_attn_shape *shape, const int32_t *widths, int32
     info->path = chosen_path() == Path::kSimt ? 1 : 0;
     info->n_splits = sp.n_splits;
     info->split_len = sp.split_len;
-    info->context_ctas = (int32_t)context_ctas(g, sp);
+    info->context_ctas = (int32_t)context_ctas(g, sp, dev.sm_count);
     info->fused_merge = (fused_merge(g, sp) || split_merge(g, sp)) ? 1 : 0;
     info->kernels = (sp.n_splits && !info->fused_merge) ? 2 : 1;
+    info->persistent = persistent(g, sp) ? 1 : 0;
     return GR_OK;
 }
 

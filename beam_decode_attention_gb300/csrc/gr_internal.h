@@ -49,6 +49,7 @@ __host__ __device__ inline int width_of(const Geometry &g, int r, int t) {
 struct SplitPlan {
     int n_splits;   // >= 1 when Lc_max > 0, 0 when there is no context
     int split_len;  // multiple of the key-block size
+    int persistent; // 1: one split on the persistent kernel (gr_ctx_pk.cu)
 };
 
 struct CtxArgs {
@@ -114,6 +115,10 @@ int tc_beams_per_tile(int G);
 int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
 int tc_merge_max_splits();      // the in-kernel split merge takes at most this many splits
 cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
+
+// gr_ctx_pk.cu  (persistent tensor-core kernel: the whole call over 128-row tiles, one key split)
+int pk_max_steps();   // chains of steps < this
+cudaError_t launch_ctx_pk(const CtxArgs &a, int sm_count, cudaStream_t s);
 
 // gr_reorder.cu  (per-beam cache reordered along BeamPath)
 cudaError_t launch_reorder(const Geometry &g, const uint16_t *beam_k, const uint16_t *beam_v,

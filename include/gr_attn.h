@@ -223,6 +223,7 @@ typedef struct {
     int32_t context_ctas;    /* CTAs of the context-stage kernel */
     int32_t kernels;         /* kernels one call launches */
     int32_t fused_merge;     /* 1 when the context kernel also runs the per-beam stage and merge */
+    int32_t persistent;      /* 1 when one persistent kernel (one CTA per SM, 128-row tiles) runs the call */
 } gr_plan_info;
 
 /*

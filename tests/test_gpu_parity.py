@@ -63,7 +63,9 @@ def test_small_workloads_every_row(name, step):
 def test_headline_workload_every_row(step):
     """The measured workload (4 requests, 2048 context keys, 900 beams) in the
     plan and launch configuration the benchmark times: every row."""
+    import beam_decode_attention_gb300 as gr
     inp, dev = workload(workloads.HEADLINE)
+    assert gr.gr_decode_attn_plan(dev.shape, dev.widths, step)["fused_merge"] == 1
     out, lse = dev.run(step, guard=64)
     ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
     compare(out, lse, ref_out, ref_lse)
@@ -158,6 +160,50 @@ def test_fused_chain_of_eight_levels():
     _run_custom(inp, steps=[5, 7], splits=1)
 
 
+@pytest.mark.parametrize("path", ["persistent", "pair"])
+def test_many_tiles_per_cta_mixed_contexts(path):
+    """More 128-row tiles than SMs, so each CTA of the persistent kernel
+    walks several items, with requests whose context is empty, one key,
+    ragged and long mixed in the same grid (items without context have no
+    key blocks; ragged tails are zeroed per ring slot) -- and the same call on
+    the tile-pair kernel."""
+    import beam_decode_attention_gb300 as gr
+    inp = workloads.make_custom(8, 16, 8, 128, [0, 1, 127, 128, 129, 0, 3000, 700], [40, 200, 300], seed=121)
+    dev = DeviceWorkload(inp)
+    os.environ["GR_ATTN_FORCE_PATH"] = path
+    try:
+        for step in range(3):
+            plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, step)
+            if plan["n_splits"] == 1:
+                assert plan["persistent"] == (0 if path == "pair" else 1)
+            out, lse = dev.run(step, guard=32)
+            ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
+            compare(out, lse, ref_out, ref_lse)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
+    assert gr.gr_get_device_error() == 0
+
+
+@pytest.mark.parametrize("step", [0, 2])
+def test_headline_on_the_persistent_kernel(step):
+    """The measured workload on the persistent kernel (480 tiles on at most
+    one CTA per SM, so each CTA takes three or four of them), which the
+    planner leaves for calls whose tiles fit one round."""
+    import beam_decode_attention_gb300 as gr
+    inp, dev = workload(workloads.HEADLINE)
+    os.environ["GR_ATTN_FORCE_PATH"] = "persistent"
+    try:
+        plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, step)
+        assert plan["persistent"] == 1 and plan["fused_merge"] == 1
+        out, lse = dev.run(step, guard=64)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
+    rows = sample_rows(inp, step, n_random=200)
+    ref_out, ref_lse, _ = ORC.decode_attn(inp, step, rows=rows)
+    idx_r = np.array([r for r, _ in rows]); idx_b = np.array([b for _, b in rows])
+    compare(out[idx_r, idx_b], lse[idx_r, idx_b], ref_out, ref_lse)
+
+
 def test_width_one():
     inp = workloads.make_custom(3, 16, 8, 128, [64, 500, 3], [1, 1, 1], seed=17)
     _run_custom(inp)
@@ -210,7 +256,8 @@ def test_tagged_beam_values():
         compare(out, lse, ref_out, ref_lse)
 
 
-def test_tagged_values_at_the_headline_geometry_fused():
+@pytest.mark.parametrize("path", ["default", "persistent"])
+def test_tagged_values_at_the_headline_geometry_fused(path):
     """The fused single-split epilogue at the headline geometry (Qwen3-0.6B
     heads, G = 2, 64 beams per 128-row tile, 900 beams: 14 full tiles and an
     8-row tail tile) with a strong signal.  Context V = 0 and each chain
@@ -230,10 +277,13 @@ def test_tagged_values_at_the_headline_geometry_fused():
     inp["beam_v"] = np.where(signs == 1, 0x3F80, 0xBF80).astype(np.uint16)   # bf16 +1 / -1
     dev = DeviceWorkload(inp)
     os.environ["GR_ATTN_FORCE_SPLITS"] = "1"
+    if path == "persistent":
+        os.environ["GR_ATTN_FORCE_PATH"] = "persistent"
     try:
         for step in range(3):
             plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, step)
             assert plan["fused_merge"] == 1 and plan["n_splits"] == 1
+            assert plan["persistent"] == (1 if path == "persistent" else 0)
             out, lse = dev.run(step, guard=64)
             ref_out, ref_lse, ref_anc = ORC.decode_attn(inp, step)
             # the signal: chain-only rows are pure +-1 mixtures, and the
@@ -244,6 +294,7 @@ def test_tagged_values_at_the_headline_geometry_fused():
             assert np.array_equal(dev.ancestors(step), ref_anc)
     finally:
         os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
     assert gr.gr_get_device_error() == 0
 
 
@@ -265,6 +316,11 @@ def test_running_max_jumps(jump):
         inp[key] = workloads.f32_to_bf16_bits(workloads.bf16_bits_to_f32(inp[key]) * 0.25)
     for splits in (1, 2):
         _run_custom(inp, steps=[0, 2], splits=splits)
+    os.environ["GR_ATTN_FORCE_PATH"] = "persistent"   # the O rescale of the persistent kernel
+    try:
+        _run_custom(inp, steps=[0, 2])
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
 
 
 def test_repeatable_and_stream():
