@@ -34,6 +34,7 @@ __all__ = [
     "gr_beam_select_workspace_size", "SELECT_MAX_WIDTH", "gr_beam_select_timed",
     "TrieSelectShape", "gr_trie_select", "gr_trie_select_workspace_size", "CtxPages",
     "gr_decode_attn_paged", "gr_beam_reorder", "gr_decode_attn_ragged",
+    "gr_beam_reorder_inplace", "gr_beam_append",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "gr_get_device_error", "gr_status_string", "gr_version", "gr_decode_attn_noalloc",
     "gr_beam_select_workspace_size", "gr_beam_select", "gr_beam_select_timed",
     "gr_trie_select_workspace_size", "gr_trie_select", "gr_decode_attn_paged", "gr_beam_reorder",
-    "gr_decode_attn_ragged",
+    "gr_decode_attn_ragged", "gr_beam_reorder_inplace", "gr_beam_append",
 )
 
 # GR_SELECT_MAX_WIDTH: the largest next_width gr_beam_select takes
@@ -185,6 +186,10 @@ def load() -> ctypes.CDLL:
     lib.gr_decode_attn_ragged.restype = ctypes.c_int
     lib.gr_beam_reorder.argtypes = [sp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
     lib.gr_beam_reorder.restype = ctypes.c_int
+    lib.gr_beam_reorder_inplace.argtypes = [sp, vp, vp, vp, vp, i32, vp]
+    lib.gr_beam_reorder_inplace.restype = ctypes.c_int
+    lib.gr_beam_append.argtypes = [sp, vp, i32, vp, vp, ctypes.c_int64, vp, vp, vp]
+    lib.gr_beam_append.restype = ctypes.c_int
     lib.gr_get_device_error.argtypes = []
     lib.gr_get_device_error.restype = ctypes.c_int
     lib.gr_status_string.argtypes = [ctypes.c_int]
@@ -425,6 +430,25 @@ def gr_beam_reorder(shape: Shape, beam_k, beam_v, beam_path, widths: Sequence[in
                                 _widths_arr(widths, step), int(step), _ptr(out_k), _ptr(out_v), _ptr(out_path),
                                 _stream_handle(stream))
     _check(rc, "gr_beam_reorder")
+
+
+def gr_beam_reorder_inplace(shape: Shape, beam_k, beam_v, beam_path, widths: Sequence[int], step: int,
+                            stream=None) -> None:
+    """The per-beam cache reordered along BeamPath in place, and the path set
+    to the identity (see ``include/gr_attn.h``)."""
+    rc = load().gr_beam_reorder_inplace(ctypes.byref(shape), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path),
+                                        _widths_arr(widths, step), int(step), _stream_handle(stream))
+    _check(rc, "gr_beam_reorder_inplace")
+
+
+def gr_beam_append(shape: Shape, widths: Sequence[int], step: int, k_new, v_new, beam_k, beam_v,
+                   src_stride: Optional[int] = None, stream=None) -> None:
+    """BeamKV append of the step's new K/V rows (see ``include/gr_attn.h``).
+    ``src_stride`` (elements between beams' rows) defaults to Hkv * D."""
+    stride = shape.num_kv_heads * shape.head_dim if src_stride is None else int(src_stride)
+    rc = load().gr_beam_append(ctypes.byref(shape), _widths_arr(widths, step), int(step), _ptr(k_new),
+                               _ptr(v_new), stride, _ptr(beam_k), _ptr(beam_v), _stream_handle(stream))
+    _check(rc, "gr_beam_append")
 
 
 def gr_get_device_error() -> int:

@@ -687,6 +687,57 @@ int gr_beam_reorder(const gr_attn_shape *shape, const void *beam_k, const void *
                                       out_path, dev.err_ptr, static_cast<cudaStream_t>(stream)));
 }
 
+int gr_beam_reorder_inplace(const gr_attn_shape *shape, void *beam_k, void *beam_v, int32_t *beam_path,
+                            const int32_t *widths, int32_t step, gr_stream_t stream) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!beam_k || !beam_v || !beam_path) return GR_ERR_NULL_ARG;
+    if (misaligned(beam_k) || misaligned(beam_v) || misaligned(beam_path)) return GR_ERR_MISALIGNED;
+    // the K and V tiles are reordered by different CTAs and the path is read
+    // by all of them: the three buffers must not share a byte
+    {
+        const size_t kv = (size_t)g.R * g.S_max * g.W_max * g.Hkv * g.D * 2;
+        const size_t path = (size_t)g.R * g.S_max * g.W_max * sizeof(int32_t);
+        if (overlaps(beam_k, kv, beam_v, kv) || overlaps(beam_k, kv, beam_path, path) ||
+            overlaps(beam_v, kv, beam_path, path))
+            return GR_ERR_BAD_SHAPE;
+    }
+    size_t smem = 0;
+    if (inplace_tile_chunks(g, &smem) == 0) return GR_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_reorder_inplace(g, static_cast<uint16_t *>(beam_k), static_cast<uint16_t *>(beam_v),
+                                              beam_path, dev.err_ptr, static_cast<cudaStream_t>(stream)));
+}
+
+int gr_beam_append(const gr_attn_shape *shape, const int32_t *widths, int32_t step, const void *k_new,
+                   const void *v_new, int64_t src_stride, void *beam_k, void *beam_v, gr_stream_t stream) {
+    Geometry g;
+    int rc = make_geometry(shape, widths, step, &g);
+    if (rc != GR_OK) return rc;
+    if (!k_new || !v_new || !beam_k || !beam_v) return GR_ERR_NULL_ARG;
+    const long long row = (long long)g.Hkv * g.D;
+    if (src_stride < row) return GR_ERR_BAD_SHAPE;
+    if (misaligned(k_new) || misaligned(v_new) || misaligned(beam_k) || misaligned(beam_v) || src_stride % 8 != 0)
+        return GR_ERR_MISALIGNED;
+    {
+        const size_t kv = (size_t)g.R * g.S_max * g.W_max * g.Hkv * g.D * 2;
+        const size_t src = ((size_t)(g.R * (long long)g.W_s - 1) * src_stride + row) * 2;
+        if (overlaps(beam_k, kv, beam_v, kv) || overlaps(k_new, src, beam_k, kv) || overlaps(k_new, src, beam_v, kv) ||
+            overlaps(v_new, src, beam_k, kv) || overlaps(v_new, src, beam_v, kv))
+            return GR_ERR_BAD_SHAPE;
+    }
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GR_OK) return rc;
+    return cuda_status(launch_append(g.R, g.W_s, g.S_max, g.W_max, g.Hkv, g.D, step,
+                                     static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+                                     (long long)src_stride, static_cast<uint16_t *>(beam_k),
+                                     static_cast<uint16_t *>(beam_v), dev.sm_count, static_cast<cudaStream_t>(stream)));
+}
+
 int gr_get_device_error(void) {
     DeviceInfo dev;
     int rc = device_info(&dev);

@@ -120,10 +120,16 @@ cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
 int pk_max_steps();   // chains of steps < this
 cudaError_t launch_ctx_pk(const CtxArgs &a, int sm_count, cudaStream_t s);
 
-// gr_reorder.cu  (per-beam cache reordered along BeamPath)
+// gr_reorder.cu  (BeamKV append; per-beam cache reordered along BeamPath)
 cudaError_t launch_reorder(const Geometry &g, const uint16_t *beam_k, const uint16_t *beam_v,
                            const int32_t *beam_path, uint16_t *out_k, uint16_t *out_v, int32_t *out_path, int *err,
                            cudaStream_t s);
+int inplace_tile_chunks(const Geometry &g, size_t *smem_bytes);   // 0: a level too wide to stage
+cudaError_t launch_reorder_inplace(const Geometry &g, uint16_t *beam_k, uint16_t *beam_v, int32_t *beam_path,
+                                   int *err, cudaStream_t s);
+cudaError_t launch_append(int R, int W_s, int S_max, int W_max, int Hkv, int D, int step, const uint16_t *k_new,
+                          const uint16_t *v_new, long long src_stride, uint16_t *beam_k, uint16_t *beam_v,
+                          int sm_count, cudaStream_t s);
 
 // gr_select.cu  (beam selection)
 size_t select_list_bytes(int R, int W, int V, int next_width);

@@ -41,7 +41,11 @@ import workloads  # noqa: E402
 METRIC = "µs/decode-step and TFLOP/s at BW=900, Lc=2048; % of bf16/HBM roofline"
 UNIT = "us/decode-step"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_tc.cu", "beam_decode_attention_gb300/csrc/gr_ptx.cuh"]
+KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_tc.cu", "beam_decode_attention_gb300/csrc/gr_tc_common.cuh",
+                  "beam_decode_attention_gb300/csrc/gr_ptx.cuh"]
+PK_KERNEL_SOURCES = ["beam_decode_attention_gb300/csrc/gr_ctx_pk.cu",
+                     "beam_decode_attention_gb300/csrc/gr_tc_common.cuh",
+                     "beam_decode_attention_gb300/csrc/gr_ptx.cuh"]
 
 
 def parse_args():
@@ -459,8 +463,10 @@ def run_trie_bench(args):
 def run_reorder_bench(args):
     """BeamPath indirection against the reordered per-beam cache (xGR's
     alternative) on the headline workload: per decode step, the attention
-    call through BeamPath, against gr_beam_reorder plus the attention call on
-    the reordered cache with the identity path.  L2 flushed before each call."""
+    call through BeamPath, against gr_beam_reorder (out of place) or
+    gr_beam_reorder_inplace plus the attention call on the reordered cache
+    with the identity path; and the BeamKV append of the step's K/V.  L2
+    flushed before each call."""
     import torch
     import beam_decode_attention_gb300 as gr
     spec = workloads.WORKLOAD_BY_NAME[workloads.HEADLINE]
@@ -483,7 +489,9 @@ def run_reorder_bench(args):
         flat = [W_s] * len(widths)
         ws = torch.empty(max(16, gr.gr_decode_attn_workspace_size(shape, widths, step)), dtype=torch.uint8,
                          device="cuda")
-        t_path, t_reorder, t_flat = [], [], []
+        t_path, t_reorder, t_flat, t_inplace, t_append = [], [], [], [], []
+        kn = torch.randn(R * W_s * spec.num_kv_heads * D, device="cuda").to(torch.bfloat16).view(torch.int16)
+        vn = torch.randn(R * W_s * spec.num_kv_heads * D, device="cuda").to(torch.bfloat16).view(torch.int16)
         for i in range(max(3, args.warmup) + args.steps):
             flush.zero_()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -497,12 +505,34 @@ def run_reorder_bench(args):
             f[1].record()
             gr.gr_decode_attn(shape, q, ck, cv, cl, ok, ov, op, flat, step, out, lse, ws)
             f[2].record()
+            # the in-place reorder on a fresh copy of the cache (a second
+            # call would find the identity path and move nothing)
+            ik, iv, ip = bk.clone(), bv.clone(), bp.clone()
+            flush.zero_()
+            h = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            h[0].record()
+            gr.gr_beam_reorder_inplace(shape, ik, iv, ip, widths, step)
+            h[1].record()
+            flush.zero_()
+            a = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            a[0].record()
+            gr.gr_beam_append(shape, widths, step, kn, vn, ik, iv)
+            a[1].record()
             torch.cuda.synchronize()
+            del ik, iv, ip
             if i >= max(3, args.warmup):
                 t_path.append(e[0].elapsed_time(e[1]) * 1000)
                 t_reorder.append(f[0].elapsed_time(f[1]) * 1000)
                 t_flat.append(f[1].elapsed_time(f[2]) * 1000)
-        res[step] = (float(np.mean(t_path)), float(np.mean(t_reorder)), float(np.mean(t_flat)))
+                t_inplace.append(h[0].elapsed_time(h[1]) * 1000)
+                t_append.append(a[0].elapsed_time(a[1]) * 1000)
+        row_bytes = spec.num_kv_heads * D * 2
+        # in place: K and V of every level below `step`, each source row read
+        # once and each beam's row written once
+        inplace_bytes = 2 * R * sum(widths[t] + W_s for t in range(step)) * row_bytes
+        append_bytes = 2 * 2 * R * W_s * row_bytes
+        res[step] = (float(np.mean(t_path)), float(np.mean(t_reorder)), float(np.mean(t_flat)),
+                     float(np.mean(t_inplace)), float(np.mean(t_append)), inplace_bytes, append_bytes)
     line = {
         "metric": "µs per decode step: attention through BeamPath vs reorder + attention on the reordered cache",
         "value": float(np.mean([v[0] for v in res.values()])), "unit": "us/decode-step", "n_gpus": 1,
@@ -510,7 +540,13 @@ def run_reorder_bench(args):
         "data": "synthetic", "config": config_of(spec, inp),
         "per_step": {str(k): {"beampath_us": round(v[0], 2), "reorder_us": round(v[1], 2),
                               "attention_on_reordered_us": round(v[2], 2),
-                              "reorder_total_us": round(v[1] + v[2], 2)} for k, v in res.items()},
+                              "reorder_total_us": round(v[1] + v[2], 2),
+                              "reorder_inplace_us": round(v[3], 2),
+                              "reorder_inplace_gbs": round(v[5] / v[3] / 1e3, 1) if v[3] > 0 else None,
+                              "inplace_total_us": round(v[3] + v[2], 2),
+                              "append_us": round(v[4], 2),
+                              "append_gbs": round(v[6] / v[4] / 1e3, 1)} for k, v in res.items()},
+        "hbm_peak_gbs": peaks().get("hbm_gbs"),
     }
     print(json.dumps(line))
     return 0
@@ -753,7 +789,10 @@ def main():
             if other.name == spec.name:
                 continue
             o = attention_run(gr, torch, other, max(3, min(args.steps, 10)), 3)
+            persistent = any(p.get("persistent") for p in o["plans"])
             per_config[other.name] = {
+                "dominant_kernel": "ctx_pk_kernel" if persistent else "ctx_tc_kernel",
+                "traffic": recorded_traffic(other.name, PK_KERNEL_SOURCES if persistent else None),
                 "us_per_decode_step": o["per_step_us"], "median_us": o["per_step_median_us"],
                 "min_us": o["per_step_min_us"], "mean_us": round(o["value"], 3), "tflops": o["tflops"],
                 "roofline_us_per_step": o["roofline_us"], "bound_per_step": o["bound"],

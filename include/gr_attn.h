@@ -404,6 +404,56 @@ int gr_beam_reorder(const gr_attn_shape *shape, const void *beam_k, const void *
                     const int32_t *beam_path, const int32_t *widths, int32_t step, void *out_k,
                     void *out_v, int32_t *out_path, gr_stream_t stream);
 
+/*
+ * The same reorder in place (xGR review, "xAttention": the unshared cache
+ * updated in place after each beam selection, so that attention reads each
+ * beam's chain from its own slots; the review's update formula is garbled,
+ * so this takes the plain reading): with the chains as for gr_beam_reorder,
+ *     beam_k/beam_v[r, t, b] <- beam_k/beam_v[r, t, a_t(b)]  for t = 0..step-1, b < widths[step]
+ *     beam_path[r, t, b]     <- b                            for t = 1..step,   b < widths[step]
+ * Level `step` (a_step = b) and beam_path[r, 0, .] are left as they are.
+ * Afterwards the caller's width schedule is widths[step] at every level
+ * t <= step: gr_decode_attn with those widths gives the rows it gave before
+ * with the old cache, path and widths.  The usual call is right after a
+ * beam selection has written the parents of step s + 1 (pass step = s + 1,
+ * before that step's K/V is appended), so the next attention call reads
+ * every chain through slot b.
+ *   beam_k, beam_v  device bf16 [R, S_max, W_max, Hkv, D], updated
+ *   beam_path       device int32 [R, S_max, W_max], read, then updated
+ * One CTA owns each column tile of a (request, level) and stages its source
+ * rows in shared memory before it writes, so no read sees a row already
+ * overwritten.  A parent outside [0, widths[t-1]) is not followed: the beam's
+ * rows below the break keep their old contents and the device error word
+ * reports GR_ERR_BAD_BEAM_PATH.  Two kernels on `stream` (none at step 0).
+ * Errors: GR_ERR_BAD_SHAPE (as gr_resolve_ancestors, or the three buffers
+ * share a byte), GR_ERR_UNSUPPORTED (a level wider than about 14,000 slots
+ * cannot be staged), GR_ERR_NULL_ARG, GR_ERR_MISALIGNED, GR_ERR_CUDA.
+ */
+int gr_beam_reorder_inplace(const gr_attn_shape *shape, void *beam_k, void *beam_v, int32_t *beam_path,
+                            const int32_t *widths, int32_t step, gr_stream_t stream);
+
+/*
+ * BeamKV append (GR-Inference blog, "system design": BeamKV holds only the
+ * short K/V each beam adds at each decode step; SID-GR README, section 3:
+ * the per-beam cache grows by one token per step): the K and V that the
+ * active beams' current tokens produced go to their own slots of the step's
+ * plane, ahead of the attention call that reads them,
+ *     beam_k[r, step, b, g, :] = k_new[(r * W_s + b) * src_stride + g * D + (0..D-1)]
+ *     beam_v[r, step, b, g, :] = v_new[... same ...]             for b < W_s = widths[step]
+ *   k_new, v_new    device bf16, R * W_s rows of Hkv * D values, row i at
+ *                   element i * src_stride (src_stride >= Hkv * D, a
+ *                   multiple of 8, so a row of a fused QKV output can be
+ *                   read where it lies)
+ *   beam_k, beam_v  device bf16 [R, S_max, W_max, Hkv, D], written at the
+ *                   rows above only
+ * One kernel on `stream`.  Errors: GR_ERR_NULL_ARG, GR_ERR_BAD_SHAPE (as
+ * gr_decode_attn, src_stride too small, or a source sharing a byte with
+ * beam_k/beam_v, or beam_k with beam_v), GR_ERR_MISALIGNED (a pointer, or
+ * src_stride not a multiple of 8), GR_ERR_UNSUPPORTED, GR_ERR_CUDA.
+ */
+int gr_beam_append(const gr_attn_shape *shape, const int32_t *widths, int32_t step, const void *k_new,
+                   const void *v_new, int64_t src_stride, void *beam_k, void *beam_v, gr_stream_t stream);
+
 /* Static description of a gr_status code. */
 const char *gr_status_string(int status);
 

@@ -208,6 +208,45 @@ def test_paged_and_reorder_reject_bad_args(lib):
     assert reorder(out_v=bk0 + 98304) not in (-1, -2, -4)         # adjacent, not overlapping: passes the checks
 
 
+def test_inplace_reorder_and_append_reject_bad_args(lib):
+    w = (ctypes.c_int32 * 3)(4, 4, 4)
+    sh = ctypes.byref(_shape())
+    MB = 1 << 20
+    kv = 98304                                  # bytes of beam_k / beam_v for this shape
+    bk0, bv0, bp0, kn0, vn0 = (FAKE + i * MB for i in range(5))
+
+    def inplace(bk=bk0, bv=bv0, bp=bp0, step=2, shape=sh, widths=w):
+        return lib.gr_beam_reorder_inplace(shape, bk, bv, bp, widths, step, None)
+
+    assert inplace(bp=None) == -1
+    assert inplace(bv=bv0 + 8) == -4
+    assert inplace(step=3) == -2                                  # step outside [0, S_max)
+    assert inplace(bv=bk0) == -2                                  # K and V the same buffer
+    assert inplace(bv=bk0 + kv - 16) == -2                        # V overlaps the end of K
+    assert inplace(bp=bv0 + 4096) == -2                           # the path inside V
+    assert inplace(bv=bk0 + kv) not in (-1, -2, -3, -4)           # adjacent: passes the checks
+    wide = (ctypes.c_int32 * 3)(15000, 15000, 15000)
+    big = ctypes.byref(_shape(beam_capacity=15000))
+    assert inplace(shape=big, widths=wide, bv=bk0 + 512 * MB, bp=bk0 + 1024 * MB) == -3   # a 15,000-slot
+    # level cannot be staged
+
+    row = 8 * 128                               # Hkv * D
+
+    def append(kn=kn0, vn=vn0, stride=row, bk=bk0, bv=bv0, step=1):
+        return lib.gr_beam_append(sh, w, step, kn, vn, stride, bk, bv, None)
+
+    assert append(kn=None) == -1
+    assert append(bv=None) == -1
+    assert append(stride=row - 8) == -2                           # rows overlap each other
+    assert append(stride=row + 4) == -4                           # rows not on 16-byte boundaries
+    assert append(vn=vn0 + 2) == -4
+    assert append(step=-1) == -2
+    assert append(kn=bk0 + 16) == -2                              # source inside the destination
+    assert append(vn=bv0 - 2 * 4 * row * 2 + 16) == -2            # source running into beam_v
+    assert append(bv=bk0) == -2
+    assert append(stride=3 * row) not in (-1, -2, -3, -4)         # a fused-QKV row stride passes
+
+
 def test_ragged_rejects_bad_args(lib):
     sh = ctypes.byref(_shape())
 

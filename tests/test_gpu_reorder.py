@@ -120,3 +120,82 @@ def test_reorder_refuses_in_place():
         gr.gr_beam_reorder(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, 1, dev.beam_k,
                            torch.empty_like(dev.beam_v), op)
     assert e.value.status == -2
+
+
+def oracle_inplace(inp, step, broken=()):
+    """The cache and path after an in-place reorder at `step`, from the
+    oracle's ancestor table: levels t < step get row b = old row a_t(b) for
+    b < W_step, levels 1..step get the identity path there, and everything
+    else keeps its old contents.  `broken` lists (r, b, t_break) beams whose
+    chain breaks at level t_break: their rows below it stay as they were."""
+    anc = ORC.ancestors(inp, step)
+    W_s = int(inp["widths"][step])
+    k, v, p = inp["beam_k"].copy(), inp["beam_v"].copy(), inp["beam_path"].copy()
+    for r in range(inp["num_requests"]):
+        for t in range(step):
+            k[r, t, :W_s] = inp["beam_k"][r, t, anc[r, :, t]]
+            v[r, t, :W_s] = inp["beam_v"][r, t, anc[r, :, t]]
+        for t in range(1, step + 1):
+            p[r, t, :W_s] = np.arange(W_s)
+    for r, b, tb in broken:
+        k[r, :tb, b] = inp["beam_k"][r, :tb, b]
+        v[r, :tb, b] = inp["beam_v"][r, :tb, b]
+    return k, v, p
+
+
+@pytest.mark.parametrize("name", ["qwen3_0.6b_r8_lc1024_w128", "qwen3_0.6b_r4_lc2048_w900",
+                                  "qwen3_1.7b_r16_lc512-4096_w20-300-900"])
+@pytest.mark.parametrize("step", [0, 1, 2])
+def test_inplace_reorder_equals_the_oracle_gather(name, step):
+    inp = workloads.make_inputs(workloads.WORKLOAD_BY_NAME[name])
+    dev = DeviceWorkload(inp)
+    gr.gr_beam_reorder_inplace(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, step)
+    torch.cuda.synchronize()
+    want_k, want_v, want_p = oracle_inplace(inp, step)
+    assert np.array_equal(_bits(dev.beam_k), want_k)
+    assert np.array_equal(_bits(dev.beam_v), want_v)
+    assert np.array_equal(_bits(dev.beam_path), want_p)
+    assert gr.gr_get_device_error() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_attention_after_inplace_reorder_gives_the_same_rows(splits):
+    inp = workloads.make_custom(2, 16, 8, 128, [300, 1000], [5, 70, 133], seed=60 + splits)
+    os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    try:
+        for step in (1, 2):
+            dev = DeviceWorkload(inp)
+            ref_out, ref_lse = dev.run(step)
+            gr.gr_beam_reorder_inplace(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, step)
+            dev.widths = [dev.widths[step]] * (step + 1) + dev.widths[step + 1:]
+            out, lse = dev.run(step)
+            assert np.array_equal(out, ref_out)
+            assert np.array_equal(lse, ref_lse)
+            assert gr.gr_get_device_error() == 0
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+
+
+def test_inplace_reorder_stops_at_a_broken_chain():
+    inp = workloads.make_custom(2, 8, 4, 64, [100, 200], [6, 40, 40], seed=71)
+    good = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in inp.items()}
+    bad = dict(good)
+    bad["beam_path"] = good["beam_path"].copy()
+    bad["beam_path"][1, 2, 7] = 40 + 3          # outside [0, W_1): the chain of (1, 7) breaks at level 2
+    dev = DeviceWorkload(bad)
+    gr.gr_beam_reorder_inplace(dev.shape, dev.beam_k, dev.beam_v, dev.beam_path, dev.widths, 2)
+    torch.cuda.synchronize()
+    assert gr.gr_get_device_error() == -8
+    # the other beams follow the intact path; beam (1, 7) keeps its levels 0 and 1
+    want_k, want_v, want_p = oracle_inplace(good, 2, broken=[(1, 7, 2)])
+    assert np.array_equal(_bits(dev.beam_k), want_k)
+    assert np.array_equal(_bits(dev.beam_v), want_v)
+    assert np.array_equal(_bits(dev.beam_path), want_p)
+
+
+def test_inplace_reorder_refuses_shared_buffers():
+    inp = workloads.make_custom(1, 4, 2, 64, [100], [2, 3], seed=2)
+    dev = DeviceWorkload(inp)
+    with pytest.raises(gr.GRError) as e:
+        gr.gr_beam_reorder_inplace(dev.shape, dev.beam_k, dev.beam_k, dev.beam_path, dev.widths, 1)
+    assert e.value.status == -2

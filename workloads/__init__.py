@@ -247,6 +247,49 @@ def make_ragged(spec: WorkloadSpec, widths: Sequence[Sequence[int]], seed: Optio
     return inp, W
 
 
+# A short decode loop: the inputs of `len(widths)` steps of append ->
+# attention -> beam selection, for one fixed context.  Recipe:
+# Generator(PCG64(seed)); draw order ctx_k, ctx_v (standard normal, bf16),
+# then per step t: k_new[t], v_new[t] ([R, W_t, Hkv, D]), q[t]
+# ([R, W_t, Hq, D]), all standard normal rounded to bf16, and for every step
+# but the last the next-token logits[t] ([R, W_t, V] float32, N(0,
+# logit_std^2)).  The loop starts from an empty BeamKV (NaN), a BeamPath of
+# -1 with step 0's parents 0, and beam scores 0.
+
+def make_decode_loop(R: int, Hq: int, Hkv: int, D: int, ctx_len: Sequence[int], widths: Sequence[int],
+                     vocab: int, logit_std: float, seed: int) -> Dict[str, object]:
+    W = tuple(int(w) for w in widths)
+    S, W_max = len(W), max(W)
+    ctx_len = np.asarray(ctx_len, dtype=np.int32)
+    lc_max = int(ctx_len.max())
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx_k = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    ctx_v = _normal_bf16(rng, (R, Hkv, lc_max, D))
+    for r in range(R):
+        ctx_k[r, :, ctx_len[r]:, :] = BF16_NAN
+        ctx_v[r, :, ctx_len[r]:, :] = BF16_NAN
+    k_new, v_new, q, logits = [], [], [], []
+    for t in range(S):
+        k_new.append(_normal_bf16(rng, (R, W[t], Hkv, D)))
+        v_new.append(_normal_bf16(rng, (R, W[t], Hkv, D)))
+        q.append(_normal_bf16(rng, (R, W[t], Hq, D)))
+        if t + 1 < S:
+            logits.append(rng.standard_normal(size=(R, W[t], vocab), dtype=np.float32) * np.float32(logit_std))
+    beam_path = np.full((R, S, W_max), -1, dtype=np.int32)
+    beam_path[:, 0, :W[0]] = 0
+    return dict(
+        name="decode_loop", num_requests=R, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+        ctx_capacity=lc_max, step_capacity=S, beam_capacity=W_max,
+        softmax_scale=float(np.float32(1.0 / np.sqrt(D))),
+        ctx_k=ctx_k, ctx_v=ctx_v, ctx_len=ctx_len,
+        beam_k=np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16),
+        beam_v=np.full((R, S, W_max, Hkv, D), BF16_NAN, dtype=np.uint16),
+        beam_path=beam_path, widths=np.asarray(W, dtype=np.int32),
+        k_new=k_new, v_new=v_new, q=q, logits=logits,
+        beam_scores=np.zeros((R, W[0]), dtype=np.float32), vocab=int(vocab),
+    )
+
+
 SELECT_HEADLINE = dict(num_requests=4, width=900, vocab=151936, next_width=900)
 
 
