@@ -66,7 +66,8 @@ constexpr int kBarODone = 2 * kStages + 5;  // [2]
 constexpr int kBarFin = 2 * kStages + 7;
 constexpr int kBarVTail = 2 * kStages + 8;     // the tail block's V rows past ctx_len are zeroed
 constexpr int kBarBeam = 2 * kStages + 9;      // chain slots and scores are in shared memory
-constexpr int kNumBars = 2 * kStages + 10;
+constexpr int kBarMerge = 2 * kStages + 10;    // [2] split merge: another split's partial tile has landed
+constexpr int kNumBars = 2 * kStages + 12;
 
 template <int D>
 struct Cfg {
@@ -92,6 +93,24 @@ struct TcParams {
     int bpt;    // beams per tile
     int tiles;  // tiles per (request, kv head)
 };
+
+// A tile's fp32 rows in shared memory as a TMA tensor copy lays them out
+// with 128-byte swizzle: D/32 column chunks of 128 rows x 128 bytes, the
+// 16-byte granule c of row m at m*128 + ((c ^ (m & 7)) << 4).  Used for the
+// split partials (stored and loaded by TMA, so that a whole tile moves in
+// one copy instead of one uncoalesced row per thread).
+__device__ __forceinline__ uint32_t f32_granule(uint32_t stg, int k, int m_local, int c) {
+    return stg + (uint32_t)(k * (kBM * 128) + m_local * 128 + ((c ^ (m_local & 7)) << 4));
+}
+__device__ __forceinline__ void st_f32x4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+__device__ __forceinline__ float4 ld_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 // One query row of the per-beam stage: its chain is walked by beam_prologue.
 struct BeamRow {
@@ -194,15 +213,15 @@ __device__ __forceinline__ void beam_prologue(const CtxArgs &a, int r, int kvh, 
 //
 // kPartial (split 0 of a call with several key splits): the merged row is
 // not final, since the other splits' context partials are still to come; it
-// is written as split 0's normalised fp32 partial and LSE instead, so that
-// the split merge (merge_splits) finds the chain folded into it.
+// goes as split 0's normalised fp32 partial into `stage`, the tile's fp32
+// staging (see f32_granule), and its LSE to *lse_part, so that the split
+// merge finds the chain folded into it.
 template <int D, bool kPartial>
 __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, long long row, bool row_ok,
                                               bool have_ctx, float m_ctx, float l_ctx, uint32_t tO,
                                               const float *s_x, const int *s_slot, const int *s_bad, int ridx,
-                                              bool beam_ok, uint32_t stage, int m_local) {
+                                              bool beam_ok, uint32_t stage, int m_local, float *lse_part = nullptr) {
     const Geometry &g = a.g;
-    float *po = kPartial ? a.part_o + row * D : nullptr;   // split 0's partial row
     auto stage_chunk = [&](int hh, int c) -> uint32_t {
         return stage + (uint32_t)(hh * (kBM * 128) + m_local * 128 + ((c ^ (m_local & 7)) << 4));
     };
@@ -236,8 +255,7 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
             if (kPartial) {
                 const float nan = __int_as_float(0x7fc00000);
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<float4 *>(po + 64 * hh + 4 * c) = make_float4(nan, nan, nan, nan);
+                for (int c = 0; c < 16; ++c) st_f32x4(f32_granule(stage, 2 * hh + (c >> 3), m_local, c & 7), nan, nan, nan, nan);
             } else {
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
@@ -287,8 +305,8 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
         if (kPartial) {
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-                *reinterpret_cast<float4 *>(po + 64 * hh + 4 * c) =
-                    make_float4(acc[4 * c + 0], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+                st_f32x4(f32_granule(stage, 2 * hh + (c >> 3), m_local, c & 7), acc[4 * c + 0], acc[4 * c + 1],
+                         acc[4 * c + 2], acc[4 * c + 3]);
         } else {
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -301,7 +319,7 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
         }
     }
     if (!row_ok) return;
-    float *lse_out = kPartial ? a.part_lse + row : a.lse + row;
+    float *lse_out = kPartial ? lse_part : a.lse + row;
     if (bad) {
         *lse_out = __int_as_float(0x7fc00000);
         if (beam_ok) raise_device_error(a.err, kDevErrBadParent);
@@ -310,97 +328,102 @@ __device__ __forceinline__ void beam_epilogue(const CtxArgs &a, int r, int kvh, 
     *lse_out = (m_tot + log2f(L)) * kLn2;
 }
 
-// The split merge, run by the 256 softmax threads of the last CTA of a
-// (request, kv head, tile pair) to finish its key split: every split has
-// written its normalised partial (O / l in fp32, LSE in natural-log units;
-// split 0's includes the chain tokens), and they are combined exactly by
-// log-sum-exp into the final bf16 row and fp32 LSE (the merging stage).
-// Phase 1, one thread per row slot: the row's LSEs (all loads in flight
-// together), their maximum M, the weights exp(lse_i - M) / sum and the final
-// LSE; the weights go to shared memory (s_w[split][slot]).  Phase 2, one warp
-// per row, lane l holding elements [l*V, l*V + V): eight rows at a time, so
-// that eight coalesced partial-row reads per split are in flight.  The
-// partials come from other CTAs, so they are read from L2 (ld.cg).  A NaN
-// partial (a broken chain) makes the row NaN.
+// The split merge of one tile, run by its 128 softmax threads in the last
+// CTA of a (request, kv head, tile pair) to finish its key split (the
+// merging stage): every split has stored its normalised partial tile (O / l
+// in fp32; split 0's includes the chain tokens) and its LSEs (natural log).
+// The thread of row m_local weighs the splits by exp(lse_i - M) / sum, M the
+// largest: each split's tile is brought into the staging area `stg` by TMA
+// (one copy per split, from L2), in split order, and every thread reads its
+// row back.  The
+// final bf16 rows go to the tile's Q tile (`out_stage`, free once the MMAs
+// are done) and leave by TMA stores; the fp32 LSE is written per row.  Every
+// named barrier is reached by all 128 threads whatever happens, so a wait
+// that gives up only records the error.  A NaN partial (a broken chain)
+// makes the row NaN.
 constexpr int kMaxMergeSplits = 16;   // splits the in-kernel merge takes
 
 template <int D>
-__device__ __forceinline__ void merge_splits(const CtxArgs &a, int r, int kvh, int tile0, bool t1_active, int bpt,
-                                             int warp8, int lane, float *s_w) {
-    constexpr int V = D / 32;
-    constexpr int kRows = 8;
+__device__ __forceinline__ void merge_tile(const CtxArgs &a, const CUtensorMap *tm_part, const CUtensorMap *tm_out,
+                                           int r, int kvh, int tile, int bpt, int t, int m_local, bool row_ok,
+                                           long long row, int sp_own, float lse_own, uint32_t stg, uint32_t mbar,
+                                           uint32_t out_stage, volatile int *abort_flag) {
     const Geometry &g = a.g;
-    const long long n_rows = (long long)g.R * g.W_s * g.Hq;
-    const int rows_per_tile = bpt * g.G;
     const int n = a.sp.n_splits;
-    // the global row of slot j (t = j / 128, m_local = j % 128), or -1
-    auto row_of = [&](int j) -> long long {
-        const int t = j / kBM, m_local = j % kBM;
-        if (t == 1 && !t1_active) return -1;
-        if (m_local >= rows_per_tile) return -1;
-        const int beam = (tile0 + t) * bpt + m_local / g.G;
-        if (beam >= width_of(g, r, g.step)) return -1;
-        return ((long long)r * g.W_s + beam) * g.Hq + kvh * g.G + m_local % g.G;
+    const long long n_rows = (long long)g.R * g.W_s * g.Hq;
+    const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
+    // the splits' LSEs (the own one is in a register, the others in L2): a
+    // first pass for their maximum M, a second for the sum of the weights;
+    // each weight is formed again where it is used
+    auto lse_of = [&](int sp) -> float {
+        if (!row_ok) return -INFINITY;
+        return sp == sp_own ? lse_own : __ldcg(a.part_lse + sp * n_rows + row);
     };
-    {
-        const int j = warp8 * 32 + lane;
-        const long long row = row_of(j);
-        if (row >= 0) {
-            float l[kMaxMergeSplits];
+    float M = -INFINITY;
+#pragma unroll 1
+    for (int sp = 0; sp < n; ++sp) M = fmaxf(M, lse_of(sp));
+    float wsum = 0.f;
+#pragma unroll 1
+    for (int sp = 0; sp < n; ++sp) wsum += exp2f((lse_of(sp) - M) * kLog2e);   // an empty split: 0; NaN stays NaN
+    float acc[D];
 #pragma unroll
-            for (int sp = 0; sp < kMaxMergeSplits; ++sp)
-                l[sp] = sp < n ? __ldcg(a.part_lse + sp * n_rows + row) : -INFINITY;
-            float M = -INFINITY;
+    for (int d = 0; d < D; ++d) acc[d] = 0.f;
+    // every split's tile (this CTA's own included, so that the sum runs in
+    // split order whichever CTA arrives last and the rows are the same in
+    // every call) comes back by TMA; the tiles were published before this
+    // CTA's acquire, which is ordered before the async-proxy loads here
+    ptx::fence_proxy_async_global();
+    int round = 0;
+#pragma unroll 1
+    for (int sp = 0; sp < n; ++sp) {
+        ptx::named_bar_sync(1 + t, 4 * 32);   // the tile's own store has read `stg`, or the previous tile has been read
+        if (quarter == 0 && lane == 0) {
+            // a box is the tile's bpt * G rows (all of them count, past W_s too)
+            ptx::mbar_arrive_expect_tx(mbar, (uint32_t)((D / 32) * bpt * g.G * 128));
 #pragma unroll
-            for (int sp = 0; sp < kMaxMergeSplits; ++sp) M = fmaxf(M, l[sp]);
-            float wsum = 0.f;
-#pragma unroll
-            for (int sp = 0; sp < kMaxMergeSplits; ++sp) {
-                l[sp] = exp2f((l[sp] - M) * kLog2e);   // an empty split (or one past n): 0
-                wsum += l[sp];
-            }
-            const float inv = 1.f / wsum;
-#pragma unroll
-            for (int sp = 0; sp < kMaxMergeSplits; ++sp)
-                if (sp < n) s_w[sp * 2 * kBM + j] = l[sp] * inv;
-            a.lse[row] = M + logf(wsum);
+            for (int k = 0; k < D / 32; ++k)
+                ptx::tma_load_4d(stg + (uint32_t)(k * kBM * 128), tm_part, mbar, 32 * k, kvh * g.G, tile * bpt,
+                                 sp * g.R + r);
         }
+        if (!wait_warp(mbar, round & 1, abort_flag)) {
+            *abort_flag = 1;
+            if (lane == 0) raise_device_error(a.err, kDevErrTimeout);
+        }
+        ++round;
+        const float ws = exp2f((lse_of(sp) - M) * kLog2e);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = ld_f32x4(f32_granule(stg, k, m_local, c));
+                acc[32 * k + 4 * c + 0] = fmaf(ws, v.x, acc[32 * k + 4 * c + 0]);
+                acc[32 * k + 4 * c + 1] = fmaf(ws, v.y, acc[32 * k + 4 * c + 1]);
+                acc[32 * k + 4 * c + 2] = fmaf(ws, v.z, acc[32 * k + 4 * c + 2]);
+                acc[32 * k + 4 * c + 3] = fmaf(ws, v.w, acc[32 * k + 4 * c + 3]);
+            }
     }
-    ptx::named_bar_sync(3, 8 * 32);
-    for (int j0 = warp8 * 32; j0 < warp8 * 32 + 32; j0 += kRows) {
-        long long row[kRows];
-        float o[kRows][V];
+    const float inv = 1.f / wsum;
+    if (row_ok) {
 #pragma unroll
-        for (int k = 0; k < kRows; ++k) {
-            row[k] = row_of(j0 + k);
+        for (int hh = 0; hh < D / 64; ++hh)
 #pragma unroll
-            for (int e = 0; e < V; ++e) o[k][e] = 0.f;
-        }
-        for (int sp = 0; sp < n; ++sp) {
-            float po[kRows][V];
-#pragma unroll
-            for (int k = 0; k < kRows; ++k) {
-                if (row[k] < 0) continue;
-                const float *src = a.part_o + (sp * n_rows + row[k]) * D + lane * V;
-                if constexpr (V == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                    po[k][0] = v.x; po[k][1] = v.y; po[k][2] = v.z; po[k][3] = v.w;
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                    po[k][0] = v.x; po[k][1] = v.y;
-                }
+            for (int c = 0; c < 8; ++c) {
+                const float *o = acc + 64 * hh + 8 * c;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 out_stage + (uint32_t)(hh * (kBM * 128) + m_local * 128 + ((c ^ (m_local & 7)) << 4))),
+                             "r"(pack_bf16x2(o[0] * inv, o[1] * inv)), "r"(pack_bf16x2(o[2] * inv, o[3] * inv)),
+                             "r"(pack_bf16x2(o[4] * inv, o[5] * inv)), "r"(pack_bf16x2(o[6] * inv, o[7] * inv))
+                             : "memory");
             }
-#pragma unroll
-            for (int k = 0; k < kRows; ++k) {
-                if (row[k] < 0) continue;
-                const float w = s_w[sp * 2 * kBM + j0 + k];
-#pragma unroll
-                for (int e = 0; e < V; ++e) o[k][e] = fmaf(w, po[k][e], o[k][e]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kRows; ++k)
-            if (row[k] >= 0) store_bf16<V>(a.out + row[k] * D + lane * V, o[k]);
+        a.lse[row] = M + logf(wsum);
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(1 + t, 4 * 32);
+    if (quarter == 0 && lane == 0) {
+        for (int h = 0; h < D / 64; ++h)
+            ptx::tma_store_4d(tm_out, out_stage + (uint32_t)(h * kBM * 128), h * 64, kvh * g.G, tile * bpt, r);
+        ptx::bulk_commit();
+        ptx::bulk_wait_all();   // the rows are written before the CTA (and its shared memory) ends
     }
 }
 
@@ -408,7 +431,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
-                  const __grid_constant__ TcParams p) {
+                  const __grid_constant__ CUtensorMap tm_part, const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -450,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarFin), 1);
         ptx::mbar_init(bar(kBarVTail), 1);
         ptx::mbar_init(bar(kBarBeam), 2);   // one arrival per beam warp
+        ptx::mbar_init(bar(kBarMerge + 0), 1);
+        ptx::mbar_init(bar(kBarMerge + 1), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -808,12 +833,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::bulk_commit();
                 ptx::bulk_wait_all();   // the rows are written before the CTA (and its shared memory) ends
             }
-        } else if (tile_active && p.a.split_merge && sp == 0) {
-            // split 0 of an in-kernel split merge: the chain is folded into its partial
-            const bool beam_ok = wait_warp(bar(kBarBeam), 0, abort_flag);
-            if (!beam_ok) fail();
-            beam_epilogue<D, true>(p.a, r, kvh, row, row_ok, ok && nb > 0, m, l, tO, s_x, s_slot, s_bad, ridx,
-                                   beam_ok, 0u, m_local);
+        } else if (p.a.split_merge) {
+            // this split's normalised partial goes to the tile's fp32 staging
+            // (ring slots 2t and 2t+1, free once the MMAs are done) and leaves by
+            // TMA; split 0 folds the chain tokens into it
+            const long long n_rows = (long long)g.R * g.W_s * g.Hq;
+            const uint32_t stg = sbase + C::kKvOff + (uint32_t)(2 * t * C::kTileBytes);
+            float lse_own = -INFINITY;
+            // the ring is free once every MMA is done: tile 1's last PV may still
+            // read a V block when tile 0's own MMAs have finished
+            if (tile_active && t == 0 && t1_active && nb > 0 && ok && !wait_warp(bar(kBarODone + 1), 0, abort_flag)) {
+                ok = false;
+                fail();
+            }
+            if (tile_active) {
+                const bool have = ok && nb > 0;
+                if (sp == 0) {
+                    const bool beam_ok = wait_warp(bar(kBarBeam), 0, abort_flag);
+                    if (!beam_ok) fail();
+                    beam_epilogue<D, true>(p.a, r, kvh, row, row_ok, have, m, l, tO, s_x, s_slot, s_bad, ridx,
+                                           beam_ok, stg, m_local, &lse_own);
+                } else {
+                    const float inv = (have && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+                    for (int q4 = 0; q4 < D / 32; ++q4) {
+                        uint32_t ov[32];
+                        if (have) {
+                            ptx::tmem_ld32(tO + 32 * q4, ov);
+                            ptx::tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) ov[j] = 0u;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            st_f32x4(f32_granule(stg, q4, m_local, c), __uint_as_float(ov[4 * c]) * inv,
+                                     __uint_as_float(ov[4 * c + 1]) * inv, __uint_as_float(ov[4 * c + 2]) * inv,
+                                     __uint_as_float(ov[4 * c + 3]) * inv);
+                    }
+                    lse_own = (have && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+                }
+                if (row_ok) p.a.part_lse[(long long)sp * n_rows + row] = lse_own;
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(1 + t, 4 * 32);
+                if (quarter == 0 && lane == 0) {
+                    for (int k = 0; k < D / 32; ++k)
+                        ptx::tma_store_4d(&tm_part, stg + (uint32_t)(k * kBM * 128), 32 * k, kvh * g.G,
+                                          (tile0 + t) * p.bpt, sp * g.R + r);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_all();
+                    ptx::fence_proxy_async_global();
+                }
+            }
+            // arrive on the (request, kv head, tile pair) counter once this CTA's
+            // partial tiles and LSEs are visible device-wide; the last split to
+            // arrive merges every split's partials into the final rows
+            volatile int *s_last = reinterpret_cast<volatile int *>(smem + C::kBarOff + kNumBars * 8 + 8);
+            __threadfence();
+            ptx::named_bar_sync(3, 8 * 32);
+            if (warp == 0 && lane == 0) {
+                const int item = (r * g.Hkv + kvh) * (int)gridDim.x + pair;
+                const int before = atomicAdd(p.a.counters + item, 1);
+                *s_last = (before == p.a.sp.n_splits - 1) ? 1 : 0;
+                __threadfence();
+            }
+            ptx::named_bar_sync(3, 8 * 32);
+            if (*s_last && tile_active) {
+                __threadfence();
+                merge_tile<D>(p.a, &tm_part, &tm_out, r, kvh, tile0 + t, p.bpt, t, m_local, row_ok, row, sp, lse_own,
+                              stg, bar(kBarMerge + t), sbase + C::kQOff + (uint32_t)(t * C::kTileBytes), abort_flag);
+            }
         } else if (tile_active) {
             const long long n_rows = (long long)g.R * g.W_s * g.Hq;
             float *po = p.a.part_o + ((long long)sp * n_rows + row) * D;
@@ -839,25 +928,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (row_ok)
                 p.a.part_lse[(long long)sp * n_rows + row] = (have && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
-        }
-        if (p.a.split_merge) {
-            // arrive on the (request, kv head, tile pair) counter once this CTA's
-            // partial rows are visible device-wide; the last split to arrive
-            // merges every split's partials into the final rows
-            volatile int *s_last = reinterpret_cast<volatile int *>(smem + C::kBarOff + kNumBars * 8 + 8);
-            __threadfence();
-            ptx::named_bar_sync(3, 8 * 32);
-            if (warp == 0 && lane == 0) {
-                const int item = (r * g.Hkv + kvh) * (int)gridDim.x + pair;
-                const int before = atomicAdd(p.a.counters + item, 1);
-                *s_last = (before == p.a.sp.n_splits - 1) ? 1 : 0;
-                __threadfence();
-            }
-            ptx::named_bar_sync(3, 8 * 32);
-            // the merge weights go to the Q tiles, free once every MMA is done
-            if (*s_last)
-                merge_splits<D>(p.a, r, kvh, tile0, t1_active, p.bpt, warp, lane,
-                                reinterpret_cast<float *>(smem + C::kQOff));
         }
     }
 
@@ -906,13 +976,25 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
     p.bpt = bpt;
     p.tiles = tiles;
     dim3 grid((tiles + 1) / 2, g.R * g.Hkv, a.sp.n_splits);
-    // fused path: the output rows leave by TMA stores with the Q tiles' geometry
-    if (a.fused) {
+    // fused path and split merge: the output rows leave by TMA stores with the
+    // Q tiles' geometry
+    if (a.fused || a.split_merge) {
         if (!encode_4d(&to, a.out, qd, qs, qb)) return cudaErrorInvalidValue;
     } else {
         to = tq;   // unused
     }
-    ctx_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, to, p);
+    // split merge: the fp32 partials [n_splits * R, W_s, Hq, D] move as tiles
+    // of 32-float column chunks
+    CUtensorMap tp;
+    if (a.split_merge) {
+        const uint64_t pd[4] = {(uint64_t)D, (uint64_t)g.Hq, (uint64_t)g.W_s, (uint64_t)a.sp.n_splits * g.R};
+        const uint64_t ps[3] = {(uint64_t)D * 4, (uint64_t)g.Hq * D * 4, (uint64_t)g.W_s * g.Hq * D * 4};
+        const uint32_t pb[4] = {32, (uint32_t)g.G, (uint32_t)bpt, 1};
+        if (!encode_4d(&tp, a.part_o, pd, ps, pb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
+    } else {
+        tp = tq;   // unused
+    }
+    ctx_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, to, tp, p);
     return cudaGetLastError();
 }
 
@@ -935,11 +1017,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode_4d(CUtensorMap *m, const void *base, const uint64_t dims[4], const uint64_t strides_bytes[3],
-               const uint32_t box[4]) {
+               const uint32_t box[4], CUtensorMapDataType dtype) {
     auto fn = encode_fn();
     if (!fn) return false;
     const uint32_t elem[4] = {1, 1, 1, 1};
-    const CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides_bytes,
+    const CUresult rc = fn(m, dtype, 4, const_cast<void *>(base), dims, strides_bytes,
                            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return rc == CUDA_SUCCESS;

@@ -96,6 +96,13 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // wait until every committed bulk store of this thread has read its shared-memory source
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) ones: after a bulk store has completed, before the release that
+// publishes it; after an acquire, before bulk loads of what it published
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // named barrier over `count` threads (whole warps)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

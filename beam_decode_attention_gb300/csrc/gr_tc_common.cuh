@@ -90,8 +90,9 @@ __device__ __forceinline__ void fma_bf16x2(float &dlo, float &dhi, uint32_t a, u
 }  // namespace tc
 
 // Host: the driver's tensor-map encoder (resolved at run time, so the library
-// loads without a driver) and a 4-D bf16 tiled map with 128-byte swizzle.
+// loads without a driver) and a 4-D tiled map with 128-byte swizzle (bf16
+// unless another element type is given).
 bool encode_4d(CUtensorMap *m, const void *base, const uint64_t dims[4], const uint64_t strides_bytes[3],
-               const uint32_t box[4]);
+               const uint32_t box[4], CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 }  // namespace gr
