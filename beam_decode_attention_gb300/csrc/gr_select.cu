@@ -10,23 +10,23 @@
 // index b * V + v ascending, and the first W' of each request give the next
 // BeamPath row (parents), the tokens and the new cumulative scores.
 //
-// Kernel 1 (select_rows_kernel), one CTA per beam row, grid-strided over the
-// rows with one CTA per SM, so that a row re-read right after its first pass
-// still sits in L2:
-//   pass 0 (HBM)  the row's maximum and sum of exponentials, and a 4096-bin
-//                 histogram of the logits' ordered bit patterns (top 12 bits),
-//                 counted only above a lower bound that tightens as the row
-//                 streams; the bin holding the row's L-th largest logit
-//                 (L = min(W', V)) bounds the candidates the row can contribute;
-//   pass 1 (L2)   every logit at or above that bin (less a margin of a few
-//                 ulps, so that candidates whose rounded scores tie with the
-//                 bin's are kept) is scored and collected in shared memory;
-//                 the row's L-th score is found among them, and those that
-//                 can still be selected are sorted by (score desc, v asc)
-//                 and written to the workspace.
-//   A row whose boundary bin holds more than the shared-memory capacity
-//   (ties, peaked or degenerate logits) takes an exact radix select on the
-//   scores instead (more passes, same result).
+// Kernel 1 (select_rows_kernel), one CTA per beam row at a time, several CTAs
+// per SM, grid-strided over the rows; every row is read from HBM once:
+//   the first logits of the row (held in registers) set a threshold, about
+//                 twice the share of the row's L best (L = min(W', V)) that
+//                 a prefix of that length holds, by a histogram of their
+//                 ordered bit patterns and a refinement inside its boundary bin;
+//   the stream    gives the row's maximum and sum of exponentials and keeps
+//                 every logit at or above the threshold in shared memory;
+//   the select    turns the kept logits into scores and finds the row's L-th
+//                 score among them; when the kept set provably holds every
+//                 logit that can reach that score (at least L kept, within
+//                 the slots, and the threshold's predecessor scoring below
+//                 it), the kept candidates that can still be selected are
+//                 sorted by (score desc, v asc) and written to the workspace.
+//   A row whose kept set is not provably complete (a skewed prefix, ties,
+//   peaked or degenerate logits) takes an exact radix select on the scores
+//   over the whole row instead (more passes, same result).
 // Each row also publishes its L-th score key (atomicMax per request): with
 // L = W' that row alone holds W' candidates at or above it, so it bounds the
 // request's W'-th score from below.
@@ -45,7 +45,8 @@ namespace gr {
 
 namespace {
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
+constexpr int kRowBlocksPerSm = 4;    // row CTAs resident per SM
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kCap = 4096;            // candidate slots per row in shared memory
@@ -227,90 +228,299 @@ __device__ __forceinline__ int compact(unsigned long long *arr, int n, int *red,
     return kept;
 }
 
-__global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) {
+// The need-th largest key among cand[0, n) (high 32 bits), by a radix select
+// in shared memory (12 + 12 + 8 bits); every thread gets it.
+__device__ __forceinline__ uint32_t radix_kth(const unsigned long long *cand, int n, int need, int *hist, int *red,
+                                              int *s_bin, int *s_above) {
+    uint32_t prefix = 0, mask = 0;
+    const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+    for (int rd = 0; rd < 3; ++rd) {
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        const int sh = shifts[rd];
+        const uint32_t bm = (1u << widths[rd]) - 1u;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint32_t k = (uint32_t)(cand[i] >> 32);
+            if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
+        }
+        __syncthreads();
+        find_bin(hist, need, red, s_bin, s_above);
+        need -= *s_above;
+        prefix |= (bm - (uint32_t)(kHistBins - 1 - *s_bin)) << sh;
+        mask |= bm << sh;
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// The exact candidate set of a row without a usable threshold: the L-th
+// largest score key of the whole row by a radix select over the row itself
+// (three more reads of it), then every larger score plus the tied ones in
+// ascending v, into cand; returns their count (at most L).
+__device__ __forceinline__ int exact_candidates(const float *z, int V, int L, float c, float S,
+                                                unsigned long long *cand, int *hist, int *red, int *s_bin,
+                                                int *s_above, int *s_cnt) {
+    uint32_t prefix = 0, mask = 0;
+    int need = L;
+    const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+    for (int rd = 0; rd < 3; ++rd) {
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        const int sh = shifts[rd];
+        const uint32_t bm = (1u << widths[rd]) - 1u;
+        for_row(z, V, [&](float x, int) {
+            const uint32_t k = ord_key(score_of(x, c, S));
+            // bins are placed at the top of the histogram so find_bin's
+            // highest-first walk works for 8-bit rounds too
+            if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
+        });
+        __syncthreads();
+        find_bin(hist, need, red, s_bin, s_above);
+        const uint32_t digit = bm - (uint32_t)(kHistBins - 1 - *s_bin);
+        need -= *s_above;
+        prefix |= digit << sh;
+        mask |= bm << sh;
+        __syncthreads();
+    }
+    const uint32_t kstar = prefix;
+    if (threadIdx.x == 0) *s_cnt = 0;
+    __syncthreads();
+    // larger keys (fewer than L) in any order; ties in ascending v, chunk by
+    // chunk so that the order is kept
+    int taken = 0;
+    for (int base = 0; base < V; base += blockDim.x) {
+        const int v = base + threadIdx.x;
+        const float x = v < V ? __ldg(z + v) : -INFINITY;
+        const uint32_t k = v < V ? ord_key(score_of(x, c, S)) : 0u;
+        if (v < V && k > kstar) {
+            const int slot = atomicAdd(s_cnt, 1);
+            if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
+        }
+        const int tie = (v < V && k == kstar) ? 1 : 0;
+        int tot;
+        const int rank = block_excl_scan(tie, red, &tot);
+        if (tie && taken + rank < need) {
+            const int slot = atomicAdd(s_cnt, 1);
+            if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
+        }
+        taken += tot;
+        if (taken >= need) {
+            // the remaining larger keys still have to be gathered
+            for (int v2 = base + blockDim.x + threadIdx.x; v2 < V; v2 += blockDim.x) {
+                const uint32_t k2 = ord_key(score_of(__ldg(z + v2), c, S));
+                if (k2 > kstar) {
+                    const int slot = atomicAdd(s_cnt, 1);
+                    if (slot < kCap) cand[slot] = pack(k2, ~(uint32_t)v2);
+                }
+            }
+            break;
+        }
+    }
+    __syncthreads();
+    return min(*s_cnt, kCap);
+}
+
+// The row's log-normaliser and candidates in one read of the row.
+//   1. The first kFirst * blockDim logits (in registers) set the threshold:
+//      the exact need_s-th largest of them (a 12-bit histogram, then a
+//      12-bit refinement inside the boundary bin), need_s about twice the
+//      share of the row's L best that a prefix of this size holds (L when
+//      the prefix is the whole row).
+//   2. The rest of the row streams from HBM once: running maximum and sum of
+//      exponentials (chunk maximum first, one rescale per chunk at most),
+//      and every logit at or above the threshold is kept as (logit key, ~v).
+//   3. With the log-normaliser c known, the candidates' logit keys become
+//      score keys and the row's L-th largest score key kl is found among
+//      them.  The set is exact when it holds at least L entries, fits its
+//      slots, and kl is above the score of the largest float below the
+//      threshold (a logit outside the set can then neither beat nor tie
+//      kl, the score being monotone in the logit).  Otherwise the row takes
+//      exact_candidates (more reads of the row, same result).
+// Then, as before: only candidates at or above max(kl, the request's
+// published bound) are kept, sorted by (score desc, v asc) and written; the
+// row publishes kl.  Several CTAs share an SM, so one row's select and sort
+// overlap another row's stream.
+constexpr int kFirst = 16;   // logits per thread in the threshold prefix
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kWarpCap = kCap / kRowWarps;   // candidate slots of each warp's region
+
+// Warp-wide: the lanes' `cnt` candidates get consecutive slots of this warp's
+// region (one shared-memory atomic per warp); returns the lane's first slot
+// (unbounded: slots past kWarpCap are not stored, the count records them).
+__device__ __forceinline__ int warp_slots(int cnt, int *wcnt) {
+    const int lane = threadIdx.x & 31;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(kFullMask, incl, 31);
+    int base = 0;
+    if (lane == 31 && total > 0) base = atomicAdd(wcnt, total);
+    base = __shfl_sync(kFullMask, base, 31);
+    return base + incl - cnt;
+}
+
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kernel(RowArgs a) {
     extern __shared__ unsigned long long sel_smem[];
     unsigned long long *cand = sel_smem;                          // [kCap]
     int *hist = reinterpret_cast<int *>(cand + kCap);             // [kHistBins]
     int *red = hist + kHistBins;                                  // [32]
     __shared__ MaxSum s_ms[kRowThreads / 32];
     __shared__ int s_bin, s_above, s_cnt;
+    __shared__ int s_wcnt[kRowWarps];   // candidates of each warp's region
     __shared__ float s_c;
+    const int warp = threadIdx.x >> 5;
+    unsigned long long *wreg = cand + warp * kWarpCap;   // this warp's region
 
     for (int row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const float *z = a.logits + (long long)row * a.V;
         const float S = a.beam_scores[row];
+        const int F = min(a.V, kFirst * (int)blockDim.x);
+
+        // 1. the threshold from the prefix [0, F)
+        float xf[kFirst];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kFirst; ++k) {
+            const int v = threadIdx.x + k * blockDim.x;
+            xf[k] = v < F ? __ldg(z + v) : -INFINITY;
+            mt = fmaxf(mt, xf[k]);
+        }
+        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+        if (threadIdx.x < kRowWarps) s_wcnt[threadIdx.x] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kFirst; ++k)
+            if (threadIdx.x + k * (int)blockDim.x < F) atomicAdd(&hist[ord_key(xf[k]) >> (32 - kHistBits)], 1);
+        __syncthreads();
+        const int need_s = a.V <= F ? a.L : min(F, 2 * (int)(((long long)F * a.L + a.V - 1) / a.V) + 16);
+        find_bin(hist, need_s, red, &s_bin, &s_above);
+        const uint32_t b_hi = (uint32_t)s_bin;
+        const int need_lo = need_s - s_above;
+        __syncthreads();
         for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-
-        // pass 0: maximum and sum of exponentials of every logit, and a
-        // histogram of the logits' keys.  Once L logits are counted, the bin
-        // holding the L-th largest of them is a lower bound on the row's
-        // boundary bin (the L-th largest of a subset is not above the row's),
-        // so later logits below it are not counted: the counts from that bin
-        // up stay exact, and most logits skip the shared-memory atomics.
-        MaxSum ms{-INFINITY, 0.f};
+#pragma unroll
+        for (int k = 0; k < kFirst; ++k) {
+            const uint32_t key = ord_key(xf[k]);
+            if (threadIdx.x + k * (int)blockDim.x < F && (key >> 20) == b_hi) atomicAdd(&hist[(key >> 8) & 0xfffu], 1);
+        }
+        __syncthreads();
+        find_bin(hist, need_lo, red, &s_bin, &s_above);
+        const uint32_t tau_key = (b_hi << 20) | ((uint32_t)s_bin << 8);
+        // keys at or below 0x7fffff hold -inf and NaN patterns: no threshold there
+        const float tau = tau_key <= 0x7fffffu ? -INFINITY : key_float(tau_key);
         {
-            int lb = 0;
-            float zg = -INFINITY;   // the smallest logit of bin lb: x >= zg <=> bin(x) >= lb
-            auto visit = [&](float x) {   // head and tail logits, before any bound
-                ms = ms_add(ms, x);
-                atomicAdd(&hist[ord_key(x) >> (32 - kHistBits)], 1);
-            };
-            const int head = min(a.V, (int)(((16 - (reinterpret_cast<uintptr_t>(z) & 15)) & 15) >> 2));
-            const int n4 = (a.V - head) >> 2, tail = head + 4 * n4;
-            for (int v = threadIdx.x; v < head; v += blockDim.x) visit(__ldg(z + v));
-            for (int v = tail + threadIdx.x; v < a.V; v += blockDim.x) visit(__ldg(z + v));
-            const float4 *row4 = reinterpret_cast<const float4 *>(z + head);
-            constexpr int kU = 8;   // 8 x 16 B in flight per thread
-            const int chunk4 = kU * blockDim.x;
-            long long seen = head + (a.V - tail);
-            for (int c0 = 0, ci = 0; c0 < n4; c0 += chunk4, ++ci) {
-                float4 x[kU];
+            int cnt = 0;
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = c0 + threadIdx.x + u * blockDim.x;
-                    if (i < n4) x[u] = __ldg(row4 + i);
-                }
-                // the chunk's maximum first, then its exponentials (independent
-                // of each other), merged into the running pair once per chunk
-                float cm = -INFINITY;
+            for (int k = 0; k < kFirst; ++k) cnt += (threadIdx.x + k * (int)blockDim.x < F && xf[k] >= tau) ? 1 : 0;
+            int slot = warp_slots(cnt, &s_wcnt[warp]);
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = c0 + threadIdx.x + u * blockDim.x;
-                    if (i >= n4) x[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                    cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
-                }
-                if (cm != -INFINITY) {
-                    // e^(x - cm) = 2^(x log2e - cm log2e): one FMA and one ex2 each
-                    const float off = -cm * kLog2e;
-                    float cs = 0.f;
-#pragma unroll
-                    for (int u = 0; u < kU; ++u)
-                        cs += (ex2_approx(fmaf(x[u].x, kLog2e, off)) + ex2_approx(fmaf(x[u].y, kLog2e, off))) +
-                              (ex2_approx(fmaf(x[u].z, kLog2e, off)) + ex2_approx(fmaf(x[u].w, kLog2e, off)));
-                    ms = ms_merge(ms, MaxSum{cm, cs});
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = c0 + threadIdx.x + u * blockDim.x;
-                    if (i < n4) {
-                        const float q[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (q[e] >= zg) atomicAdd(&hist[ord_key(q[e]) >> (32 - kHistBits)], 1);
-                    }
-                }
-                seen += 4LL * min(chunk4, n4 - c0);
-                // tighten the bound after chunks 0, 1, 3 and 7
-                if (seen >= a.L && c0 + chunk4 < n4 && (ci & (ci + 1)) == 0 && ci < 8) {
-                    __syncthreads();
-                    find_bin(hist, a.L, red, &s_bin, &s_above);
-                    lb = s_bin;
-                    // bins at or below 7 hold -inf and NaN patterns: no bound there
-                    zg = lb <= 7 ? -INFINITY : key_float((uint32_t)lb << (32 - kHistBits));
+            for (int k = 0; k < kFirst; ++k) {
+                const int v = threadIdx.x + k * blockDim.x;
+                if (v < F && xf[k] >= tau) {
+                    if (slot < kWarpCap) wreg[slot] = pack(ord_key(xf[k]), ~(uint32_t)v);
+                    ++slot;
                 }
             }
         }
+        // the prefix's exponentials, against the thread's maximum so far
+        float acc = 0.f;
+        if (mt != -INFINITY) {
+            const float off = -mt * kLog2e;
+#pragma unroll
+            for (int k = 0; k < kFirst; ++k) acc += ex2_approx(fmaf(xf[k], kLog2e, off));
+        }
+
+        // 2. the rest of the row, once: 16-byte loads where the row allows
+        {
+            const float *zr = z + F;
+            const int Vr = a.V - F;
+            const int head = min(Vr, (int)(((16 - (reinterpret_cast<uintptr_t>(zr) & 15)) & 15) >> 2));
+            const int n4 = (Vr - head) >> 2, tail = head + 4 * n4;
+            auto one = [&](float x, int v) {   // a logit outside the 16-byte body
+                if (x > mt) {
+                    acc = (mt == -INFINITY ? 0.f : acc * ex2_approx((mt - x) * kLog2e)) + 1.f;
+                    mt = x;
+                } else if (x != -INFINITY) {
+                    acc += ex2_approx((x - mt) * kLog2e);
+                }
+                if (x >= tau) {
+                    const int slot = atomicAdd(&s_wcnt[warp], 1);
+                    if (slot < kWarpCap) wreg[slot] = pack(ord_key(x), ~(uint32_t)v);
+                }
+            };
+            for (int v = threadIdx.x; v < head; v += blockDim.x) one(__ldg(zr + v), F + v);
+            for (int v = tail + threadIdx.x; v < Vr; v += blockDim.x) one(__ldg(zr + v), F + v);
+            const float4 *row4 = reinterpret_cast<const float4 *>(zr + head);
+            // kU 16-byte loads per thread per step, and the next step's loads
+            // issued before this step's logits are used (2 * kU in flight)
+            constexpr int kU = 4;
+            const int step = kU * blockDim.x;
+            auto load = [&](float4 (&x)[kU], int c0) {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = c0 + threadIdx.x + u * blockDim.x;
+                    x[u] = i < n4 ? __ldg(row4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+            };
+            auto use = [&](const float4 (&x)[kU], int c0) {
+                float cm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) cm = fmaxf(cm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+                if (cm > mt) {
+                    acc = mt == -INFINITY ? 0.f : acc * ex2_approx((mt - cm) * kLog2e);
+                    mt = cm;
+                }
+                if (mt != -INFINITY) {
+                    const float off = -mt * kLog2e;
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        acc += (ex2_approx(fmaf(x[u].x, kLog2e, off)) + ex2_approx(fmaf(x[u].y, kLog2e, off))) +
+                               (ex2_approx(fmaf(x[u].z, kLog2e, off)) + ex2_approx(fmaf(x[u].w, kLog2e, off)));
+                }
+                // only lanes whose step holds a candidate take this path (about a
+                // quarter of them): one atomic on the warp's own counter per lane,
+                // then the lane's candidates in order (the -inf fill past the
+                // body is never a candidate, even when the threshold is -inf)
+                if (cm >= tau) {
+                    int cnt = 0;
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        if (c0 + (int)threadIdx.x + u * (int)blockDim.x < n4)
+                            cnt += (x[u].x >= tau) + (x[u].y >= tau) + (x[u].z >= tau) + (x[u].w >= tau);
+                    if (cnt > 0) {
+                        int slot = atomicAdd(&s_wcnt[warp], cnt);
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int i4 = c0 + threadIdx.x + u * blockDim.x;
+                            const int v = F + head + 4 * i4;
+                            const float q[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (i4 < n4 && q[e] >= tau) {
+                                    if (slot < kWarpCap) wreg[slot] = pack(ord_key(q[e]), ~(uint32_t)(v + e));
+                                    ++slot;
+                                }
+                        }
+                    }
+                }
+            };
+            float4 xa[kU], xb[kU];
+            load(xa, 0);
+            for (int c0 = 0; c0 < n4; c0 += 2 * step) {
+                load(xb, c0 + step);
+                use(xa, c0);
+                if (c0 + step >= n4) break;
+                load(xa, c0 + 2 * step);
+                use(xb, c0 + step);
+            }
+        }
+        MaxSum ms{mt, acc};
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
@@ -322,125 +532,61 @@ __global__ void __launch_bounds__(kRowThreads, 1) select_rows_kernel(RowArgs a) 
             MaxSum t = s_ms[0];
             for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
             s_c = t.m + __logf(t.s);   // log-normaliser c_b
-            s_cnt = 0;
         }
-        find_bin(hist, a.L, red, &s_bin, &s_above);
-        const float c = s_c;
-
-        // pass 1: candidates at or above the boundary bin, less a margin that
-        // keeps every logit whose rounded score could tie with the bin's
-        const float zlo = key_float((uint32_t)s_bin << (32 - kHistBits));
-        const float margin = (fabsf(c) + fabsf(S) + fabsf(zlo) + 1.f) * 0x1p-19f;
-        // a boundary bin below -inf (W' past the row's finite logits) decodes to
-        // a NaN pattern: then every logit is a candidate
-        const float zthr = zlo >= -3.402823466e38f ? zlo - margin : -INFINITY;
-        for_row(z, a.V, [&](float x, int v) {
-            if (x >= zthr) {
-                const int slot = atomicAdd(&s_cnt, 1);
-                if (slot < kCap) cand[slot] = pack(ord_key(score_of(x, c, S)), ~(uint32_t)v);
-            }
-        });
         __syncthreads();
-        int n = s_cnt;
-        if (n > kCap) {
-            // Exact radix select of the L-th largest score key (12 + 12 + 8
-            // bits), then every larger score plus the tied ones in v order.
-            uint32_t prefix = 0, mask = 0;
-            int need = a.L;
-            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
-#pragma unroll
-            for (int rd = 0; rd < 3; ++rd) {
-                for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
-                __syncthreads();
-                const int sh = shifts[rd];
-                const uint32_t bm = (1u << widths[rd]) - 1u;
-                for_row(z, a.V, [&](float x, int) {
-                    const uint32_t k = ord_key(score_of(x, c, S));
-                    // bins are placed at the top of the histogram so find_bin's
-                    // highest-first walk works for 8-bit rounds too
-                    if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
-                });
-                __syncthreads();
-                find_bin(hist, need, red, &s_bin, &s_above);
-                const uint32_t digit = bm - (uint32_t)(kHistBins - 1 - s_bin);
-                need -= s_above;
-                prefix |= digit << sh;
-                mask |= bm << sh;
-                __syncthreads();
-            }
-            const uint32_t kstar = prefix;
-            if (threadIdx.x == 0) s_cnt = 0;
-            __syncthreads();
-            // larger keys (fewer than L) in any order; ties in ascending v,
-            // chunk by chunk so that the order is kept
-            int taken = 0;
-            for (int base = 0; base < a.V; base += blockDim.x) {
-                const int v = base + threadIdx.x;
-                const float x = v < a.V ? __ldg(z + v) : -INFINITY;
-                const uint32_t k = v < a.V ? ord_key(score_of(x, c, S)) : 0u;
-                if (v < a.V && k > kstar) {
-                    const int slot = atomicAdd(&s_cnt, 1);
-                    if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
-                }
-                const int tie = (v < a.V && k == kstar) ? 1 : 0;
-                int tot;
-                const int rank = block_excl_scan(tie, red, &tot);
-                if (tie && taken + rank < need) {
-                    const int slot = atomicAdd(&s_cnt, 1);
-                    if (slot < kCap) cand[slot] = pack(k, ~(uint32_t)v);
-                }
-                taken += tot;
-                if (taken >= need) {
-                    // the remaining larger keys still have to be gathered
-                    for (int v2 = base + blockDim.x + threadIdx.x; v2 < a.V; v2 += blockDim.x) {
-                        const uint32_t k2 = ord_key(score_of(__ldg(z + v2), c, S));
-                        if (k2 > kstar) {
-                            const int slot = atomicAdd(&s_cnt, 1);
-                            if (slot < kCap) cand[slot] = pack(k2, ~(uint32_t)v2);
-                        }
-                    }
-                    break;
-                }
-            }
-            __syncthreads();
-            n = min(s_cnt, kCap);
+        const float c = s_c;
+        // the warps' regions become one array: every warp reads its entries
+        // into registers, and after a barrier writes them at its offset
+        int n = 0, off = 0;
+        bool overflow = false;
+        for (int w = 0; w < kRowWarps; ++w) {
+            const int cw = s_wcnt[w];
+            overflow |= cw > kWarpCap;
+            if (w < warp) off += min(cw, kWarpCap);
+            n += min(cw, kWarpCap);
         }
-        // The row's L-th largest score key among the n candidates (radix
-        // select in shared memory).  With L = W' this row alone holds W'
-        // candidates at or above it, so it bounds the request's W'-th score
-        // from below: it is published, and no candidate under the larger of
-        // it and the bound published so far can be selected, so only those
-        // at or above are kept (the row's best, at most L of them).
-        uint32_t kl = 0u;
         {
-            uint32_t prefix = 0, mask = 0;
-            int need = a.L;
-            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+            constexpr int kPer = kWarpCap / 32;
+            const int lane = threadIdx.x & 31, cw = min(s_wcnt[warp], kWarpCap);
+            unsigned long long ent[kPer];
 #pragma unroll
-            for (int rd = 0; rd < 3; ++rd) {
-                for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
-                __syncthreads();
-                const int sh = shifts[rd];
-                const uint32_t bm = (1u << widths[rd]) - 1u;
-                for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                    const uint32_t k = (uint32_t)(cand[i] >> 32);
-                    if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
-                }
-                __syncthreads();
-                find_bin(hist, need, red, &s_bin, &s_above);
-                need -= s_above;
-                prefix |= (bm - (uint32_t)(kHistBins - 1 - s_bin)) << sh;
-                mask |= bm << sh;
-                __syncthreads();
-            }
-            kl = prefix;
+            for (int j = 0; j < kPer; ++j) ent[j] = lane + 32 * j < cw ? wreg[lane + 32 * j] : 0ull;
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (lane + 32 * j < cw) cand[off + lane + 32 * j] = ent[j];
+            __syncthreads();
         }
+        if (overflow) n = kCap + 1;
+
+        // 3. score keys, the row's L-th, and whether the set is exact
+        uint32_t kl = 0u;
+        bool exact = n >= a.L && n <= kCap;
+        if (exact) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const unsigned long long e = cand[i];
+                cand[i] = pack(ord_key(score_of(key_float((uint32_t)(e >> 32)), c, S)), (uint32_t)e);
+            }
+            __syncthreads();
+            kl = radix_kth(cand, n, a.L, hist, red, &s_bin, &s_above);
+            if (tau != -INFINITY) {
+                const float below = nextafterf(tau, -INFINITY);
+                exact = kl > ord_key(score_of(below, c, S));
+            }
+        }
+        if (!exact) {
+            n = exact_candidates(z, a.V, a.L, c, S, cand, hist, red, &s_bin, &s_above, &s_cnt);
+            kl = radix_kth(cand, n, a.L, hist, red, &s_bin, &s_above);
+        }
+        // Only candidates at or above the larger of kl and the request's
+        // published bound can be selected (kl bounds the request's W'-th score
+        // from below when L = W'): keep those (the row's best, at most L of
+        // them, plus ties), sort and write them.
         uint32_t keep = kl;
         if (a.tau_lb) {
             const uint32_t lbnow = *reinterpret_cast<volatile unsigned *>(a.tau_lb + row / a.W);
             keep = lbnow > keep ? lbnow : keep;
         }
-        // compact the candidates with key >= keep to the front, chunk by chunk
         int kept = 0;
         for (int base = 0; base < n; base += blockDim.x) {
             const int i = base + threadIdx.x;
@@ -871,7 +1017,8 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ra.V = V;
     ra.L = L;
     const int smem = kCap * 8 + kHistBins * 4 + 32 * 4;
-    const int grid = ra.rows < sm_count[dev] ? ra.rows : sm_count[dev];
+    const int slots = sm_count[dev] * kRowBlocksPerSm;
+    const int grid = ra.rows < slots ? ra.rows : slots;
     select_rows_kernel<<<grid, kRowThreads, smem, s>>>(ra);
     e = cudaGetLastError();
     if (e == cudaSuccess && between) e = cudaEventRecord(between, s);

@@ -104,6 +104,30 @@ def test_constant_rows_take_the_exact_fallback():
     assert np.allclose(sco[0], -1.0 - np.log(20000.0), atol=1e-5)
 
 
+@pytest.mark.parametrize("skew", ["prefix_high", "prefix_low", "tail_high", "mixed_scales", "prefix_masked"])
+def test_threshold_prefix_skews(skew):
+    """The row kernel sets its candidate threshold from each row's first
+    logits: rows whose prefix is not representative (its best far above or
+    below the rest, or rows of different scales) must still select exactly,
+    through the completeness check or the exact fallback."""
+    R, W, V, n = 2, 24, 20000, 64
+    inp = workloads.make_select_inputs(R, W, V, seed={"prefix_high": 1, "prefix_low": 2, "tail_high": 3,
+                                                      "mixed_scales": 4, "prefix_masked": 5}[skew])
+    z = inp["logits"]
+    if skew == "prefix_high":
+        z[:, :, :4096] += np.float32(3.0)
+    elif skew == "prefix_low":
+        z[:, :, :4096] -= np.float32(10.0)
+    elif skew == "tail_high":
+        z[:, :, 15000:] += np.float32(6.0)
+    elif skew == "prefix_masked":
+        z[:, :, :4096] = -np.inf
+    else:
+        z[:, ::2, :] *= np.float32(0.05)
+    par, tok, sco, _ = run_select(z, inp["beam_scores"], n)
+    check(z, inp["beam_scores"], n, par, tok, sco)
+
+
 def test_masked_tokens_and_width_past_the_finite_candidates():
     """-inf logits mask tokens; asking for more beams than there are finite
     candidates returns the finite ones by score, then masked ones by index."""
