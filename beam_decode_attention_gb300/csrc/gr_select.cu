@@ -205,6 +205,67 @@ __device__ __forceinline__ void bitonic_desc(unsigned long long *a, int n) {
         }
 }
 
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+    const uint32_t lo = __shfl_xor_sync(kFullMask, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(kFullMask, (uint32_t)(v >> 32), m);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+// The same descending bitonic sort with the elements in registers: thread t
+// holds elements t + q * blockDim (q < n / blockDim, or one element for
+// t < n when n <= blockDim), exchanges at strides below 32 are warp shuffles
+// (no barrier) and larger strides go through shared memory.  n is a power of
+// two, 64 <= n <= 4 * blockDim, blockDim a multiple of 32.
+__device__ __forceinline__ void bitonic_desc_shfl(unsigned long long *a, int n) {
+    constexpr int kMaxPer = 4;
+    const int bd = blockDim.x, t = threadIdx.x, lane = t & 31;
+    const int per = n > bd ? n / bd : 1;
+    const bool active = t < n;   // n >= 64 is a multiple of 32: whole warps are in or out
+    unsigned long long x[kMaxPer];
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) x[q] = (q < per && active) ? a[t + q * bd] : 0ull;
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            if (jj >= 32) {
+                __syncthreads();   // the previous stage's reads are done
+#pragma unroll
+                for (int q = 0; q < kMaxPer; ++q)
+                    if (q < per && active) a[t + q * bd] = x[q];
+                __syncthreads();
+#pragma unroll
+                for (int q = 0; q < kMaxPer; ++q) {
+                    if (!(q < per && active)) continue;
+                    const int i = t + q * bd, pi = i ^ jj;
+                    const unsigned long long o = a[pi];
+                    const bool take_max = ((i & k) == 0) == (i < pi);
+                    x[q] = take_max ? (o > x[q] ? o : x[q]) : (o < x[q] ? o : x[q]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kMaxPer; ++q) {
+                    if (q >= per) continue;   // uniform across the block
+                    const int i = t + q * bd;
+                    const unsigned long long o = shfl_xor_u64(x[q], jj);
+                    const bool take_max = ((i & k) == 0) == ((lane & jj) == 0);
+                    x[q] = take_max ? (o > x[q] ? o : x[q]) : (o < x[q] ? o : x[q]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q)
+        if (q < per && active) a[t + q * bd] = x[q];
+    __syncthreads();
+}
+
+// Descending sort of n (a power of two) values: in registers where the
+// shuffle form takes n, else the shared-memory network.
+__device__ __forceinline__ void sort_desc(unsigned long long *a, int n) {
+    if (n >= 64 && n <= 4 * (int)blockDim.x) bitonic_desc_shfl(a, n);
+    else bitonic_desc(a, n);
+}
+
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t low) {
     return ((unsigned long long)key << 32) | low;
 }
@@ -602,7 +663,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         while (np2 < kept) np2 <<= 1;
         for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
         __syncthreads();
-        bitonic_desc(cand, np2);
+        sort_desc(cand, np2);
         const int cnt = min(kept, a.L);
         unsigned long long *out = a.lists + (long long)row * a.L;
         for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = cand[j];
@@ -633,7 +694,8 @@ struct MergeSelArgs {
 // dynamic shared memory of the merge kernel: list offsets, per-list counts
 // above and tied with the threshold, the histogram and the selection
 constexpr int kMaxBeams = 4096;   // GR_SELECT_MAX_BEAMS
-constexpr int kMergeSmem = (3 * (kMaxBeams + 1) + kHistBins) * 4 + kMaxSel * 8;
+constexpr int kEntCap = 4096;     // entries the merge holds in shared memory at once
+constexpr int kMergeSmem = (3 * (kMaxBeams + 1) + kHistBins) * 4 + (kMaxSel + kEntCap) * 8;
 
 // One CTA per request.  Each row list holds the row's best candidates down to
 // the bound that row saw; only entries at or above the final lower bound can
@@ -646,7 +708,8 @@ constexpr int kMergeSmem = (3 * (kMaxBeams + 1) + kHistBins) * 4 + kMaxSel * 8;
 __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSelArgs a) {
     extern __shared__ unsigned long long msm[];
     unsigned long long *sel = msm;                           // [kMaxSel] (8-byte entries first)
-    int *offs = reinterpret_cast<int *>(sel + kMaxSel);      // [W + 1]
+    unsigned long long *ent = sel + kMaxSel;                 // [kEntCap] the candidates at or above the bound
+    int *offs = reinterpret_cast<int *>(ent + kEntCap);      // [W + 1]
     int *gtc = offs + (kMaxBeams + 1);                       // [W + 1] entries above tau, then offsets
     int *eqc = gtc + (kMaxBeams + 1);                        // [W + 1] entries tied with tau, then offsets
     int *hist = eqc + (kMaxBeams + 1);                       // [kHistBins]
@@ -660,16 +723,18 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     const int b0 = min(a.W, (int)threadIdx.x * per), b1 = min(a.W, b0 + per);
     // A tighter bound: the next_width-th largest key among the first kh keys
     // of every list (real candidates, so at least next_width entries reach it).
+    const int kh = min(32, max(1, (4 * a.next_width + a.W - 1) / a.W));
+    // the keys go where offs, gtc and eqc will be (not yet in use)
+    const unsigned *heads = reinterpret_cast<const unsigned *>(offs);
+    const bool have_heads = a.W * kh <= 3 * (kMaxBeams + 1);
     {
-        const int kh = min(32, max(1, (4 * a.next_width + a.W - 1) / a.W));
-        // the keys go where offs, gtc and eqc will be (not yet in use)
-        unsigned *heads = reinterpret_cast<unsigned *>(offs);
+        unsigned *heads_w = reinterpret_cast<unsigned *>(offs);
         const int cap = 3 * (kMaxBeams + 1);
         int nh = 0;
         if (a.W * kh <= cap) {
             for (int t = threadIdx.x; t < a.W * kh; t += blockDim.x) {
                 const int b = t / kh, j = t % kh;
-                heads[t] = j < plen[b] ? (unsigned)(lists[(long long)b * a.L + j] >> 32) : 0u;
+                heads_w[t] = j < plen[b] ? (unsigned)(lists[(long long)b * a.L + j] >> 32) : 0u;
             }
             nh = a.W * kh;
         }
@@ -698,25 +763,48 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
             lb = prefix > lb ? prefix : lb;
         }
     }
-    // per list, the sorted prefix at or above the bound (binary search), then
-    // the list offsets: lists [b0, b1) of this thread are consecutive
+    // per list, the sorted prefix at or above the bound: from the head keys
+    // when the prefix ends among them (most lists), else by a binary search
+    // past them; then the list offsets (lists [b0, b1) of this thread are
+    // consecutive, at most 4 of them).  The head keys share memory with the
+    // offsets: every thread reads them before the scan's barriers, and the
+    // offsets are written after it.
+    int pl[4] = {0, 0, 0, 0};
     int mine = 0;
-    for (int b = b0; b < b1; ++b) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int b = b0 + q;
+        if (b >= b1) break;
         const unsigned long long *lst = lists + (long long)b * a.L;
-        int lo = 0, hi = plen[b];   // first index whose key < lb
+        const int len = plen[b];
+        int lo = 0;
+        if (have_heads) {
+            const int hn = min(kh, len);
+            while (lo < hn && heads[b * kh + lo] >= lb) ++lo;
+            if (lo < hn || len <= kh) {
+                pl[q] = lo;
+                mine += lo;
+                continue;
+            }
+        }
+        int hi = len;   // first index whose key < lb
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             if ((uint32_t)(lst[mid] >> 32) >= lb) lo = mid + 1;
             else hi = mid;
         }
-        gtc[b] = lo;   // the prefix length, for now
+        pl[q] = lo;
         mine += lo;
     }
     int total;
     int off = block_excl_scan(mine, red, &total);
-    for (int b = b0; b < b1; ++b) {
+    __syncthreads();   // every head key has been read
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int b = b0 + q;
+        if (b >= b1) break;
         offs[b] = off;
-        off += gtc[b];
+        off += pl[q];
         gtc[b] = 0;
         eqc[b] = 0;
     }
@@ -733,6 +821,71 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         b = lo;
         j = e - offs[lo];
     };
+    // the W' selected entries, sorted by (score desc, flat asc), into the outputs
+    auto emit = [&](const unsigned long long *src, int n_sel) {
+        for (int j = threadIdx.x; j < a.next_width; j += blockDim.x) {
+            int32_t pb = -1, tv = -1, nd = -1;
+            float sc = -INFINITY;
+            if (j < n_sel) {
+                const unsigned long long e = src[j];
+                const uint32_t flat = ~(uint32_t)e;
+                pb = (int32_t)(flat / (uint32_t)a.V);
+                tv = (int32_t)(flat % (uint32_t)a.V);
+                sc = key_float((uint32_t)(e >> 32));
+                if (a.next_node) {
+                    // the edge of the parent's node that carries the token; the node
+                    // and its edge range are checked as the rows kernel checks them,
+                    // and a search that lands past the range or on another token (a
+                    // node whose tokens are not increasing) gives no child
+                    const int n = a.beam_node[(long long)r * a.W + pb];
+                    if (n >= 0 && n < a.num_nodes) {
+                        const int e0 = a.trie_offsets[n], e1 = a.trie_offsets[n + 1];
+                        if (e0 >= 0 && e1 <= a.num_edges && e0 <= e1) {
+                            int lo = e0, hi = e1;
+                            while (lo < hi) {
+                                const int mid = (lo + hi) >> 1;
+                                if (a.trie_tokens[mid] < tv) lo = mid + 1;
+                                else hi = mid;
+                            }
+                            if (lo < e1 && a.trie_tokens[lo] == tv) nd = a.trie_children[lo];
+                        }
+                    }
+                }
+            }
+            a.next_parent[(long long)r * a.parent_stride + j] = pb;
+            a.next_token[(long long)r * a.next_width + j] = tv;
+            a.next_score[(long long)r * a.next_width + j] = sc;
+            if (a.next_node) a.next_node[(long long)r * a.next_width + j] = nd;
+        }
+    };
+    if (total <= kEntCap) {
+        // Every candidate at or above the bound fits in shared memory: read each
+        // once as (score key, ~flat index), find the n_sel-th largest key tau,
+        // keep the entries at or above it and sort them; the first n_sel are
+        // the selection (ties at tau in flat-index order, as the sort puts them).
+        for (int e = threadIdx.x; e < total; e += blockDim.x) {
+            int b, j;
+            locate(e, b, j);
+            const unsigned long long v = lists[(long long)b * a.L + j];
+            const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)v;
+            ent[e] = ((v >> 32) << 32) | (uint32_t)~flat;
+        }
+        __syncthreads();
+        const int n_sel = min(a.next_width, total);
+        int kept = 0;
+        if (n_sel > 0) {
+            const uint32_t tau = radix_kth(ent, total, n_sel, hist, red, &s_bin, &s_above);
+            kept = compact(ent, total, red, [&](unsigned long long e) { return (uint32_t)(e >> 32) >= tau; },
+                           [](unsigned long long e) { return e; });
+        }
+        int np2 = 1;
+        while (np2 < kept) np2 <<= 1;
+        for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) ent[i] = 0ull;
+        __syncthreads();
+        sort_desc(ent, np2);
+        emit(ent, n_sel);
+        return;
+    }
     constexpr int kIn = 4;   // loads in flight per thread
     // radix select of the n_sel-th largest key (n_sel < next_width only when
     // the request has fewer candidates: the rest of the slots are padding)
@@ -821,41 +974,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     while (np2 < a.next_width) np2 <<= 1;
     for (int i = n_sel + threadIdx.x; i < np2; i += blockDim.x) sel[i] = 0ull;
     __syncthreads();
-    bitonic_desc(sel, np2);
-    for (int j = threadIdx.x; j < a.next_width; j += blockDim.x) {
-        int32_t pb = -1, tv = -1, nd = -1;
-        float sc = -INFINITY;
-        if (j < n_sel) {
-            const unsigned long long e = sel[j];
-            const uint32_t flat = ~(uint32_t)e;
-            pb = (int32_t)(flat / (uint32_t)a.V);
-            tv = (int32_t)(flat % (uint32_t)a.V);
-            sc = key_float((uint32_t)(e >> 32));
-            if (a.next_node) {
-                // the edge of the parent's node that carries the token; the node
-                // and its edge range are checked as the rows kernel checks them,
-                // and a search that lands past the range or on another token (a
-                // node whose tokens are not increasing) gives no child
-                const int n = a.beam_node[(long long)r * a.W + pb];
-                if (n >= 0 && n < a.num_nodes) {
-                    const int e0 = a.trie_offsets[n], e1 = a.trie_offsets[n + 1];
-                    if (e0 >= 0 && e1 <= a.num_edges && e0 <= e1) {
-                        int lo = e0, hi = e1;
-                        while (lo < hi) {
-                            const int mid = (lo + hi) >> 1;
-                            if (a.trie_tokens[mid] < tv) lo = mid + 1;
-                            else hi = mid;
-                        }
-                        if (lo < e1 && a.trie_tokens[lo] == tv) nd = a.trie_children[lo];
-                    }
-                }
-            }
-        }
-        a.next_parent[(long long)r * a.parent_stride + j] = pb;
-        a.next_token[(long long)r * a.next_width + j] = tv;
-        a.next_score[(long long)r * a.next_width + j] = sc;
-        if (a.next_node) a.next_node[(long long)r * a.next_width + j] = nd;
-    }
+    sort_desc(sel, np2);
+    emit(sel, n_sel);
 }
 
 // ---------------------------------------------------------------- item-constrained rows
@@ -878,14 +998,139 @@ struct TrieRowArgs {
     unsigned long long *lists;   // [R * W_s][W'] sorted descending
     int *plen;
     unsigned *tau_lb;
+    int *big_count;              // rows whose node has more edges than a warp holds
+    int *big_rows;               // [R * W_s] those rows, in any order
     int rows, W, V, next_width, num_nodes, num_edges;
 };
 
+// A row's trie node and its edge range [p0, p1) (empty for a node index or
+// edge range outside the trie).
+__device__ __forceinline__ void node_edges(const TrieRowArgs &a, int row, int &p0, int &p1) {
+    const int n = a.beam_node[row];
+    p0 = 0;
+    p1 = 0;
+    if (n >= 0 && n < a.num_nodes) {
+        p0 = a.offsets[n];
+        p1 = a.offsets[n + 1];
+        if (p0 < 0 || p1 > a.num_edges || p1 < p0) p0 = p1 = 0;
+    }
+}
+
+// One warp per beam row whose node has at most kTrieWarpDeg edges (8 per
+// lane): the legal logits are gathered in one round trip, the masked
+// log-normaliser comes from warp reductions, and the row's candidates
+// (score key, ~v) are sorted by a bitonic network in registers (lane l holds
+// elements 8l..8l+7; exchanges across lanes are shuffles), so a row costs no
+// block barrier.  The best min(W', degree) are written as the block kernel
+// writes them.  Rows with more edges are appended to big_rows for
+// trie_rows_kernel.
+constexpr int kTrieWarpDeg = 256;
+constexpr int kTrieWarpRows = 8;   // rows (warps) per CTA
+
+__global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(TrieRowArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kTrieWarpRows + (threadIdx.x >> 5);
+    if (row >= a.rows) return;   // warp-uniform
+    int p0, p1;
+    node_edges(a, row, p0, p1);
+    const int deg = p1 - p0;
+    if (deg > kTrieWarpDeg) {
+        if (lane == 0) a.big_rows[atomicAdd(a.big_count, 1)] = row;
+        return;
+    }
+    const float *z = a.logits + (long long)row * a.V;
+    const float S = a.beam_scores[row];
+    // lane l takes edges 8l .. 8l+7
+    int v[8];
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int k = 8 * lane + j;
+        v[j] = k < deg ? a.tokens[p0 + k] : -1;
+        if (v[j] >= a.V) v[j] = -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = v[j] >= 0 ? __ldg(z + v[j]) : -INFINITY;
+    MaxSum ms{-INFINITY, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (v[j] >= 0) ms = ms_add(ms, x[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
+        ms = ms_merge(ms, other);
+    }
+    const float c = ms.m + __logf(ms.s);
+    // a skipped edge sorts last and is not kept: key 0 is below every score
+    unsigned long long e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) e[j] = v[j] >= 0 ? pack(ord_key(score_of(x[j], c, S)), ~(uint32_t)v[j]) : 0ull;
+    // descending bitonic sort of the warp's 256 elements (index i = 8 * lane + j)
+#pragma unroll
+    for (int k = 2; k <= kTrieWarpDeg; k <<= 1) {
+#pragma unroll
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            if (jj >= 8) {
+                const int m = jj >> 3;
+                const bool lower = (lane & m) == 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = 8 * lane + j;
+                    const bool desc = (i & k) == 0;
+                    const unsigned long long o = shfl_xor_u64(e[j], m);
+                    const bool take_max = desc == lower;
+                    e[j] = take_max ? (o > e[j] ? o : e[j]) : (o < e[j] ? o : e[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int pj = j ^ jj;
+                    if (pj > j) {
+                        const int i = 8 * lane + j;
+                        const bool desc = (i & k) == 0;
+                        const unsigned long long lo = e[j], hi = e[pj];
+                        const bool sw = desc ? (lo < hi) : (lo > hi);
+                        e[j] = sw ? hi : lo;
+                        e[pj] = sw ? lo : hi;
+                    }
+                }
+            }
+        }
+    }
+    // the kept count: valid candidates, at most W'
+    int valid = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) valid += (e[j] >> 32) != 0ull ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(kFullMask, valid, o);
+    const int cnt = min(valid, a.next_width);
+    unsigned long long *out = a.lists + (long long)row * a.next_width;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (8 * lane + j < cnt) out[8 * lane + j] = e[j];
+    if (lane == 0) a.plen[row] = cnt;
+    // a row with W' candidates of its own bounds the request's W'-th score
+    if (cnt == a.next_width && cnt > 0 && a.tau_lb) {   // warp-uniform
+        const int jl = (cnt - 1) & 7;
+        unsigned long long pick = e[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            if (j == jl) pick = e[j];
+        const unsigned long long last = __shfl_sync(kFullMask, pick, (cnt - 1) >> 3);
+        if (lane == 0) atomicMax(a.tau_lb + row / a.W, (unsigned)(last >> 32));
+    }
+}
+
+// The rows whose node has more edges than a warp holds, one CTA at a time per
+// row (grid-strided over big_rows).
 __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) {
     __shared__ unsigned long long buf[kMaxSel + kTrieChunk];
     __shared__ MaxSum s_ms[kTrieThreads / 32];
     __shared__ float s_c;
-    const int row = blockIdx.x;
+    __shared__ int s_keep;
+    const int nbig = *reinterpret_cast<volatile int *>(a.big_count);
+    for (int bi = blockIdx.x; bi < nbig; bi += gridDim.x) {
+    const int row = a.big_rows[bi];
     const int n = a.beam_node[row];
     int p0 = 0, p1 = 0;
     if (n >= 0 && n < a.num_nodes) {
@@ -939,7 +1184,6 @@ __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) 
         cnt = min(tot, L);
     }
     // drop skipped edges (key 0) from the kept count
-    __shared__ int s_keep;
     if (threadIdx.x == 0) {
         int k = cnt;
         while (k > 0 && (buf[k - 1] >> 32) == 0ull) --k;
@@ -953,6 +1197,8 @@ __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) 
         a.plen[row] = cnt;
         // a row with W' candidates of its own bounds the request's W'-th score
         if (cnt == a.next_width && a.tau_lb) atomicMax(a.tau_lb + row / a.W, (unsigned)(buf[cnt - 1] >> 32));
+    }
+    __syncthreads();   // buf and the shared scalars are reused by the next row
     }
 }
 
@@ -1039,8 +1285,12 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     return cudaGetLastError();
 }
 
+// trie workspace: row lists [R * W][W'] u64 | lower bounds [R] u32 and the
+// big-row count (16-byte padded) | list lengths [R * W] int32 | big rows [R * W] int32
+static size_t trie_bound_bytes(int R) { return ((size_t)(R + 1) * 4 + 15) / 16 * 16; }
+
 size_t trie_select_bytes(int R, int W, int next_width) {
-    return list_bytes(R, W, next_width) + bound_bytes(R) + (size_t)R * W * sizeof(int);
+    return list_bytes(R, W, next_width) + trie_bound_bytes(R) + 2 * (size_t)R * W * sizeof(int);
 }
 
 cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_nodes, int num_edges,
@@ -1050,23 +1300,29 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
                                float *next_score, int32_t *next_node, void *workspace, cudaStream_t s,
                                cudaEvent_t between) {
     static std::mutex mu;
-    static bool attr_set[64] = {};
+    static int sm_count[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lk(mu);
-        if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(select_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+        if (sm_count[dev] == 0) {
+            int nsm = 0;
+            e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(select_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
             if (e != cudaSuccess) return e;
-            attr_set[dev] = true;
+            sm_count[dev] = nsm;
         }
     }
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
     unsigned *tau_lb = reinterpret_cast<unsigned *>(wsb + list_bytes(R, W, next_width));
-    int *plen = reinterpret_cast<int *>(wsb + list_bytes(R, W, next_width) + bound_bytes(R));
-    e = cudaMemsetAsync(tau_lb, 0, (size_t)R * 4, s);
+    int *big_count = reinterpret_cast<int *>(tau_lb + R);
+    int *plen = reinterpret_cast<int *>(wsb + list_bytes(R, W, next_width) + trie_bound_bytes(R));
+    int *big_rows = plen + (size_t)R * W;
+    // the bounds and the big-row count start at zero (one copy)
+    e = cudaMemsetAsync(tau_lb, 0, (size_t)(R + 1) * 4, s);
     if (e != cudaSuccess) return e;
     TrieRowArgs ta;
     ta.logits = logits;
@@ -1083,7 +1339,15 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ta.next_width = next_width;
     ta.num_nodes = num_nodes;
     ta.num_edges = num_edges;
-    trie_rows_kernel<<<R * W, kTrieThreads, 0, s>>>(ta);
+    ta.big_count = big_count;
+    ta.big_rows = big_rows;
+    trie_rows_warp_kernel<<<(R * W + kTrieWarpRows - 1) / kTrieWarpRows, kTrieWarpRows * 32, 0, s>>>(ta);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    {
+        const int grid = R * W < 2 * sm_count[dev] ? R * W : 2 * sm_count[dev];
+        trie_rows_kernel<<<grid, kTrieThreads, 0, s>>>(ta);
+    }
     e = cudaGetLastError();
     if (e == cudaSuccess && between) e = cudaEventRecord(between, s);
     if (e != cudaSuccess) return e;

@@ -158,8 +158,9 @@ def _tsel(**kw):
 
 
 def test_trie_select_workspace_and_bad_args(lib):
-    # per beam row a list of next_width 8-byte entries and its length; a bound per request
-    assert lib.gr_trie_select_workspace_size(ctypes.byref(_tsel())) == 2 * 4 * 8 * 8 + 16 + 2 * 4 * 4
+    # per beam row a list of next_width 8-byte entries, its length and a slot in the list of
+    # rows too wide for one warp; a bound per request and that list's count (16-byte padded)
+    assert lib.gr_trie_select_workspace_size(ctypes.byref(_tsel())) == 2 * 4 * 8 * 8 + 16 + 2 * (2 * 4 * 4)
     for bad in (dict(num_nodes=0), dict(num_edges=-1), dict(next_width=1025), dict(width=4097)):
         assert lib.gr_trie_select_workspace_size(ctypes.byref(_tsel(**bad))) == 0, bad
 

@@ -95,6 +95,19 @@ def test_node_with_more_edges_than_a_chunk():
     check(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], 1000, got)
 
 
+def test_rows_wide_and_narrow_in_one_request():
+    """Beams at a node with more edges than one warp holds (the block kernel)
+    and beams at small nodes (the warp kernel) in the same requests: both
+    feed one merge."""
+    t = workloads.make_sid_trie(4000, 2, 600, 2000, seed=91)   # the root has ~600 edges
+    assert t["offsets"][1] > 256
+    inp = workloads.make_trie_select_inputs(2, 10, 2000, t, 1, seed=92)
+    bn = inp["beam_node"].copy()
+    bn[:, ::3] = 0   # every third beam at the root
+    got = run(inp["logits"], inp["beam_scores"], bn, t["offsets"], t["tokens"], t["children"], 40)
+    check(inp["logits"], inp["beam_scores"], bn, t["offsets"], t["tokens"], t["children"], 40, got)
+
+
 def test_out_of_range_nodes_are_skipped():
     """Beams whose node index lies outside the trie contribute nothing (the
     kernel checks the index before reading the trie)."""
