@@ -789,7 +789,9 @@ def main():
             if other.name == spec.name:
                 continue
             o = attention_run(gr, torch, other, max(3, min(args.steps, 10)), 3)
-            persistent = any(p.get("persistent") for p in o["plans"])
+            # the kernel of the slowest decode step dominates the call
+            slowest = int(np.argmax(o["per_step_us"]))
+            persistent = bool(o["plans"][slowest].get("persistent"))
             per_config[other.name] = {
                 "dominant_kernel": "ctx_pk_kernel" if persistent else "ctx_tc_kernel",
                 "traffic": recorded_traffic(other.name, PK_KERNEL_SOURCES if persistent else None),
