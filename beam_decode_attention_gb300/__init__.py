@@ -278,15 +278,18 @@ def gr_decode_attn_paged(shape: Shape, pages: CtxPages, q, ctx_k_pool, ctx_v_poo
 def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
                          widths: Sequence[int], step: int, out, lse, workspace, events,
                          workspace_bytes: Optional[int] = None, stream=None) -> None:
-    """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``)
-    before the context kernel, after it, and after the last kernel."""
+    """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``
+    or None, which is not recorded) before the context kernel, after it, and
+    after the last kernel."""
     w = _widths_arr(widths, step)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if len(events) != 3:
+        raise ValueError("events: three torch.cuda.Event or None")
     for e in events:
-        if e.cuda_event == 0:      # torch creates the event lazily on first record
+        if e is not None and e.cuda_event == 0:      # torch creates the event lazily on first record
             e.record()
-    ev = (ctypes.c_void_p * 3)(*[int(e.cuda_event) for e in events])
+    ev = (ctypes.c_void_p * 3)(*[0 if e is None else int(e.cuda_event) for e in events])
     rc = load().gr_decode_attn_timed(ctypes.byref(shape), _ptr(q), _ptr(ctx_k), _ptr(ctx_v),
                                      _ptr(ctx_len), _ptr(beam_k), _ptr(beam_v), _ptr(beam_path), w,
                                      int(step), _ptr(out), _ptr(lse), _ptr(workspace),

@@ -17,8 +17,9 @@
 // Consecutive items and key blocks overlap:
 //   TMEM    S_0 [0,128) S_1 [128,256): S of consecutive key blocks (global
 //           block n uses S_{n&1}), so S(n+1) is computed while the softmax
-//           of block n runs; O_0 [256,256+D) O_1 [256+D,256+2D): item u
-//           accumulates in O_{u&1} while the epilogue drains item u-1's.
+//           of block n runs; O [256,256+D): the item's context partial;
+//           C [256+D,256+2D): the partial of the rows' own chains, written by
+//           the epilogue warps while the context loop runs.
 //   SMEM    the item's Q tile (reloaded once its last S is done and its
 //           chains are scored); a 3-slot K ring and a 3-slot V ring that
 //           run on across items, so a K block is in flight for about two
@@ -27,10 +28,12 @@
 //   warps 0-3   softmax, one thread per row (TMEM lane): online max / sum,
 //               P (bf16) over the first 64 columns of S_{n&1}; the O
 //               rescale is rare (kSumLimit) and waits for the previous PV.
-//   warps 4-7   epilogue, one thread per row: walks the row's chain and
-//               scores its tokens (in registers) while the item's context
-//               loop runs, then merges context partial and chain tokens and
-//               writes the bf16 row and its LSE.
+//   warps 4-7   epilogue, one thread per row: while the item's context
+//               loop runs, walks the row's chain, scores its tokens and
+//               accumulates their V rows into C (a softmax of its own, with
+//               the chain's maximum and sum kept in registers); once O is
+//               complete, merges the two partials by log-sum-exp from TMEM
+//               and writes the bf16 row and its LSE.
 //   warp 8      TMA producer of the Q tiles and the K ring.
 //   warp 9      MMA issuer (one lane).
 //   warp 10     TMA producer of the V ring (zeroes V rows past ctx_len).
@@ -82,13 +85,13 @@ constexpr int kBarQFreeS = 16;       // the issuer is done with an item's Q tile
 constexpr int kBarQFreeE = 17;       // the epilogue has scored an item's chains (4 warps)
 constexpr int kBarSFull = 18;        // [2] S_b computed
 constexpr int kBarPFull = 20;        // [2] P over S_b written (4 softmax warps)
-constexpr int kBarOFull = 22;        // [2] O_b holds the item's context partial
-constexpr int kBarOEmpty = 24;       // [2] O_b read by the epilogue (4 warps)
-constexpr int kBarStats = 26;        // the item's row max / sum written (4 softmax warps)
-constexpr int kBarStatsFree = 27;    // the epilogue has read them (4 warps)
-constexpr int kBarPvDone = 28;       // one phase per PV
-constexpr int kBarFin = 29;
-constexpr int kNumBars = 30;
+constexpr int kBarOFull = 22;        // O holds the item's context partial
+constexpr int kBarOEmpty = 23;       // O read by the epilogue (4 warps)
+constexpr int kBarStats = 24;        // the item's row max / sum written (4 softmax warps)
+constexpr int kBarStatsFree = 25;    // the epilogue has read them (4 warps)
+constexpr int kBarPvDone = 26;       // one phase per PV
+constexpr int kBarFin = 27;
+constexpr int kNumBars = 28;
 
 template <int D>
 struct PkCfg {
@@ -104,7 +107,8 @@ struct PkCfg {
     static constexpr int kUsed = kStats + 2 * kBM * 4;
     static constexpr int kSmem = kUsed + 1024;
     static constexpr int kSCol = 0;                     // S_b at kSCol + b * kBN
-    static constexpr int kOCol = 2 * kBN;               // O_b at kOCol + b * D
+    static constexpr int kOCol = 2 * kBN;               // context partial O
+    static constexpr int kCCol = 2 * kBN + D;           // chain partial C
 };
 
 struct PkParams {
@@ -140,7 +144,8 @@ __device__ __forceinline__ Item item_of(const PkParams &p, int k) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_pk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PkParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                  const __grid_constant__ PkParams p) {
     using C = PkCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,9 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(bar(kBarSFull + b), 1);
                 ptx::mbar_init(bar(kBarPFull + b), 4);
-                ptx::mbar_init(bar(kBarOFull + b), 1);
-                ptx::mbar_init(bar(kBarOEmpty + b), 4);
             }
+            ptx::mbar_init(bar(kBarOFull), 1);
+            ptx::mbar_init(bar(kBarOEmpty), 4);
             ptx::mbar_init(bar(kBarStats), 4);
             ptx::mbar_init(bar(kBarStatsFree), 4);
             ptx::mbar_init(bar(kBarPvDone), 1);
@@ -336,13 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n = 0;          // global block of the next PV
             int u = 0;          // active items so far (Q phases)
             int zpar = 0;       // bit s: parity of the next zeroing of V slot s
-            int ocnt = 0;       // items with context so far that used O_0 (bits 0-15) / O_1 (bits 16-31)
+            int oc = 0;         // items with context so far (one O phase each)
             for (int j = 0; ok && j < n_mine; ++j) {
                 const Item it = item_of(p, item_k(j));
                 if (!it.active) continue;
-                const int b = u & 1;
                 if (it.nb == 0) {
-                    // no context: nothing to issue, O_b is not touched.  Its Q phase is
+                    // no context: nothing to issue, O is not touched.  Its Q phase is
                     // still awaited and released in turn (a commit, so that it completes
                     // after the previous item's last S), keeping both in order.
                     if (!(ok = wait_lane(bar(kBarQFull), (uint32_t)(u & 1), abort_flag))) break;
@@ -350,17 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++u;
                     continue;
                 }
-                const int oc = (ocnt >> (16 * b)) & 0xffff;   // earlier items with context on O_b
-                ocnt += 1 << (16 * b);
                 for (int i = 0; i < it.nb; ++i, ++n) {
                     // S(n) and, within the item, S(n + 1) -- which goes into the S
                     // buffer that PV(n - 1) has read -- before P(n) is awaited
                     if (sn == n && !(ok = issue_s(i == 0, i == it.nb - 1, u))) break;
                     if (sn == n + 1 && i + 1 < it.nb && !(ok = issue_s(false, i + 1 == it.nb - 1, u))) break;
                     if (!(ok = wait_lane(bar(kBarPFull + (n & 1)), (uint32_t)((n >> 1) & 1), abort_flag))) break;
-                    // the item's first PV overwrites O_b: the epilogue must have read the
-                    // previous item with context on O_b
-                    if (i == 0 && oc > 0 && !(ok = wait_lane(bar(kBarOEmpty + b), (uint32_t)((oc - 1) & 1), abort_flag)))
+                    // the item's first PV overwrites O: the epilogue must have read the
+                    // previous item's
+                    if (i == 0 && oc > 0 && !(ok = wait_lane(bar(kBarOEmpty), (uint32_t)((oc - 1) & 1), abort_flag)))
                         break;
                     const int slot = n % kVStages;
                     const bool ragged = (i == it.nb - 1) && it.tail < kBN;
@@ -371,14 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ragged) zpar ^= 1 << slot;
                     ptx::tc_fence_after();
                     const uint64_t b0 = dv0 + (uint64_t)slot * kSlot;
-                    const uint32_t d = tmem + C::kOCol + (uint32_t)b * D, a = tmem + C::kSCol + (uint32_t)(n & 1) * kBN;
+                    const uint32_t d = tmem + C::kOCol, a = tmem + C::kSCol + (uint32_t)(n & 1) * kBN;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         ptx::mma_ts(d, a + kk * 8, b0 + (uint64_t)(kk * (2048 >> 4)), kIdescPV, (kk > 0 || i > 0) ? 1u : 0u);
                     ptx::mma_commit(bar(kBarVEmpty + slot));
                     ptx::mma_commit(bar(kBarPvDone));
-                    if (i == it.nb - 1) ptx::mma_commit(bar(kBarOFull + b));
+                    if (i == it.nb - 1) ptx::mma_commit(bar(kBarOFull));
                 }
+                ++oc;
                 ++u;
             }
             if (!ok) fail();
@@ -392,17 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const float c = g.scale_log2;
         float *s_stats = reinterpret_cast<float *>(smem + C::kStats);
+        const uint32_t tO = tmem + lane_off + (uint32_t)C::kOCol;
         bool ok = true;
         int n = 0;
-        int u = 0;
         int sc = 0;   // items with context so far (one stats phase each)
         for (int j = 0; ok && j < n_mine; ++j) {
             const Item it = item_of(p, item_k(j));
             if (!it.active) continue;
-            const int b = u & 1;
-            ++u;
             if (it.nb == 0) continue;   // no context: no blocks, no row statistics
-            const uint32_t tO = tmem + lane_off + (uint32_t)(C::kOCol + b * D);
             float m = -INFINITY, l = 0.f;
             for (int i = 0; i < it.nb; ++i, ++n) {
                 const int valid = (i == it.nb - 1) ? it.tail : kBN;
@@ -505,16 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp - kEpiWarp0;
         const int m_local = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_off + (uint32_t)C::kOCol;
+        const uint32_t tC = tmem + lane_off + (uint32_t)C::kCCol;
         const float *s_stats = reinterpret_cast<const float *>(smem + C::kStats);
         const uint32_t q_row = sbase + C::kQOff + (uint32_t)m_local * 128u;
         const int swz = m_local & 7;
+        // the CTA's last active item writes its rows through the Q tile (free once
+        // its last S has completed, with no further Q to load) and TMA stores;
+        // earlier items store their rows directly
+        int j_last = n_mine - 1;
+        while (j_last >= 0 && !item_of(p, item_k(j_last)).active) --j_last;
         int u = 0;
-        int sc = 0;     // items with context so far (stats phases)
-        int ocnt = 0;   // items with context so far that used O_0 (bits 0-15) / O_1 (bits 16-31)
+        int sc = 0;     // items with context so far (stats and O phases)
         for (int j = 0; j < n_mine; ++j) {
             const Item it = item_of(p, item_k(j));
             if (!it.active) continue;
-            const int b = u & 1;
+            const bool staged = j == j_last;
             const int beam = it.tile * p.bpt + m_local / g.G;
             const bool row_ok = m_local < rows_per_tile && beam < width_of(g, it.r, g.step);
             const long long row = ((long long)it.r * g.W_s + beam) * g.Hq + it.kvh * g.G + m_local % g.G;
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // fetching each token's parent index and K row in one round trip, and
             // score the token against the row's query (base-2 units).  A parent
             // outside [0, W_{t-1}) is not followed: the row is flagged and nothing
-            // past it is read.  The V rows are prefetched into L2 for the merge.
+            // past it is read.  The V rows are prefetched into L2 for the chain partial.
             float x[kMaxTokens];
             int slot_of[kMaxTokens];
             bool chain_ok = true;
@@ -568,14 +574,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the Q tile may be reloaded for the next item
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarQFreeE));
+            // The chain's own partial, still while the context loop runs: its
+            // maximum m_c, weights w_t = 2^(x_t - m_c) and sum l_c in registers,
+            // and C = sum_t w_t v_t in TMEM, one token's V row at a time.  TMEM is
+            // read and written by the whole warp; rows without a chain add zeros.
+            const bool chain = row_ok && ok && chain_ok;
+            float m_c = -INFINITY;
+#pragma unroll
+            for (int tt = 0; tt < kMaxTokens; ++tt) m_c = fmaxf(m_c, x[tt]);   // unused levels hold -inf
+            float w[kMaxTokens];
+            float l_c = 0.f;
+#pragma unroll
+            for (int tt = 0; tt < kMaxTokens; ++tt) {
+                w[tt] = chain ? ptx::ex2(x[tt] - m_c) : 0.f;
+                l_c += w[tt];
+            }
+#pragma unroll 1
+            for (int tt = 0; tt <= g.step; ++tt) {
+                // this token's weight and slot, picked from the register tables
+                float wt = w[0];
+                int st = slot_of[0];
+#pragma unroll
+                for (int k = 1; k < kMaxTokens; ++k) {
+                    wt = tt == k ? w[k] : wt;
+                    st = tt == k ? slot_of[k] : st;
+                }
+                const uint4 *rv = reinterpret_cast<const uint4 *>(
+                    p.a.beam_v + ((((long long)it.r * g.S_max + tt) * g.W_max + st) * g.Hkv + it.kvh) * D);
+                uint4 v[D / 8];
+#pragma unroll
+                for (int ch = 0; ch < D / 8; ++ch) v[ch] = chain ? __ldg(rv + ch) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t acc[32];
+                    if (tt > 0) {
+                        ptx::tmem_ld32(tC + 32 * q, acc);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] = 0u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint4 &vc = v[4 * q + (e >> 2)];
+                        const uint32_t vw = (e & 3) == 0 ? vc.x : (e & 3) == 1 ? vc.y : (e & 3) == 2 ? vc.z : vc.w;
+                        acc[2 * e] = __float_as_uint(fmaf(wt, __uint_as_float(vw << 16), __uint_as_float(acc[2 * e])));
+                        acc[2 * e + 1] =
+                            __float_as_uint(fmaf(wt, __uint_as_float(vw & 0xffff0000u), __uint_as_float(acc[2 * e + 1])));
+                    }
+                    ptx::tmem_st32(tC + 32 * q, acc);
+                }
+                ptx::tmem_wait_st();
+            }
             // the context partial (items with context only)
             float m_ctx = -INFINITY, l_ctx = 0.f;
             bool have_ctx = false;
             if (it.nb > 0) {
-                const uint32_t par = (uint32_t)(ocnt >> (16 * b)) & 1u;
                 ok = wait_warp(bar(kBarStats), (uint32_t)(sc & 1), abort_flag) && ok;
-                ok = wait_warp(bar(kBarOFull + b), par, abort_flag) && ok;
-                ocnt += 1 << (16 * b);
+                ok = wait_warp(bar(kBarOFull), (uint32_t)(sc & 1), abort_flag) && ok;
                 ++sc;
                 have_ctx = ok;
                 if (have_ctx) {
@@ -587,78 +643,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) fail();
             ptx::tc_fence_after();
+            // log-sum-exp merge of the context partial (O, m_ctx, l_ctx) and the
+            // chain partial (C, m_c, l_c)
             const bool bad = row_ok && (!ok || !chain_ok);
-            float m_tot = m_ctx;
-            if (row_ok && !bad) {
-#pragma unroll
-                for (int tt = 0; tt < kMaxTokens; ++tt) m_tot = fmaxf(m_tot, x[tt]);   // unused levels hold -inf
-            }
-            const float w_ctx = ptx::ex2(m_ctx - m_tot);   // no context: exp2(-inf) = 0
-            float L = l_ctx * w_ctx;
-            float pw[kMaxTokens];
-#pragma unroll
-            for (int tt = 0; tt < kMaxTokens; ++tt) {
-                pw[tt] = (row_ok && !bad) ? ptx::ex2(x[tt] - m_tot) : 0.f;
-                L += pw[tt];
-            }
-            const float inv = row_ok && !bad ? 1.f / L : 0.f;
-            const float wc = w_ctx * inv;
-            const uint32_t tO = tmem + lane_off + (uint32_t)(C::kOCol + b * D);
+            const bool good = row_ok && !bad;
+            const float m_tot = fmaxf(m_ctx, m_c);
+            const float w_ctx = good ? ptx::ex2(m_ctx - m_tot) : 0.f;   // no context: exp2(-inf) = 0
+            const float w_ch = good ? ptx::ex2(m_c - m_tot) : 0.f;
+            const float L = l_ctx * w_ctx + l_c * w_ch;
+            const float inv = good ? 1.f / L : 0.f;
+            const float wc = w_ctx * inv, wh = w_ch * inv;
             uint16_t *orow = p.a.out + row * D;
 #pragma unroll 1
-            for (int hh = 0; hh < D / 64; ++hh) {
-                float acc[64];
-                if (have_ctx) {
-                    ptx::tmem_ld32(tO + 64 * hh, reinterpret_cast<uint32_t *>(&acc[0]));
-                    ptx::tmem_ld32(tO + 64 * hh + 32, reinterpret_cast<uint32_t *>(&acc[32]));
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int d = 0; d < 64; ++d) acc[d] = 0.f;
-                }
-                if (hh == D / 64 - 1 && it.nb > 0) {
-                    // O_b is read: the next item with context on it may accumulate into it
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32], cc[32];
+                if (have_ctx) ptx::tmem_ld32(tO + 32 * q, o);
+                ptx::tmem_ld32(tC + 32 * q, cc);
+                ptx::tmem_wait_ld();
+                if (q == D / 32 - 1 && it.nb > 0) {
+                    // O is read: the next item with context may accumulate into it
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + b));
+                    if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty));
                 }
                 if (!row_ok) continue;
+                uint32_t pk[16];
                 if (bad) {
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        reinterpret_cast<uint4 *>(orow + 64 * hh)[cc] =
-                            make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-                    continue;
-                }
+                    for (int e = 0; e < 16; ++e) pk[e] = 0x7fc07fc0u;   // NaN marks a row whose chain is broken
+                } else {
 #pragma unroll
-                for (int d = 0; d < 64; ++d) acc[d] *= wc;
-                // chain tokens one at a time (their V rows were prefetched into L2)
-#pragma unroll
-                for (int tt = 0; tt < kMaxTokens; ++tt) {
-                    if (tt > g.step) continue;
-                    const float pt = pw[tt] * inv;
-                    const uint4 *rv = reinterpret_cast<const uint4 *>(
-                        p.a.beam_v +
-                        ((((long long)it.r * g.S_max + tt) * g.W_max + slot_of[tt]) * g.Hkv + it.kvh) * D + 64 * hh);
-                    uint4 va[8];
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) va[cc] = __ldg(rv + cc);
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint32_t ua[4] = {va[cc].x, va[cc].y, va[cc].z, va[cc].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            acc[8 * cc + 2 * e] = fmaf(pt, __uint_as_float(ua[e] << 16), acc[8 * cc + 2 * e]);
-                            acc[8 * cc + 2 * e + 1] =
-                                fmaf(pt, __uint_as_float(ua[e] & 0xffff0000u), acc[8 * cc + 2 * e + 1]);
-                        }
+                    for (int e = 0; e < 16; ++e) {
+                        const float a0 = have_ctx ? __uint_as_float(o[2 * e]) * wc : 0.f;
+                        const float a1 = have_ctx ? __uint_as_float(o[2 * e + 1]) * wc : 0.f;
+                        pk[e] = pack_bf16x2(fmaf(__uint_as_float(cc[2 * e]), wh, a0),
+                                            fmaf(__uint_as_float(cc[2 * e + 1]), wh, a1));
                     }
                 }
+                if (staged) {
+                    // columns 32q.. of the row: half q/2, 16-byte chunks 4(q&1).. of its
+                    // 128-byte swizzled line, as the output tensor map lays a box out
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc)
-                    reinterpret_cast<uint4 *>(orow + 64 * hh)[cc] =
-                        make_uint4(pack_bf16x2(acc[8 * cc + 0], acc[8 * cc + 1]), pack_bf16x2(acc[8 * cc + 2], acc[8 * cc + 3]),
-                                   pack_bf16x2(acc[8 * cc + 4], acc[8 * cc + 5]), pack_bf16x2(acc[8 * cc + 6], acc[8 * cc + 7]));
+                    for (int k = 0; k < 4; ++k) {
+                        const int chunk = 4 * (q & 1) + k;
+                        const uint32_t addr = q_row + (uint32_t)(q >> 1) * (kBM * 128) + (uint32_t)((chunk ^ swz) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * k]),
+                                     "r"(pk[4 * k + 1]), "r"(pk[4 * k + 2]), "r"(pk[4 * k + 3])
+                                     : "memory");
+                    }
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * q);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                }
+            }
+            if (staged) {
+                // the tile's rows leave by TMA (rows past W_s or past the tile's
+                // beams are outside the box or the tensor and are not written)
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(1, 4 * 32);
+                if (quarter == 0 && lane == 0) {
+                    for (int h = 0; h < C::kHalves; ++h)
+                        ptx::tma_store_4d(&tm_out, sbase + C::kQOff + h * C::kHalfBytes, h * 64, it.kvh * g.G,
+                                          it.tile * p.bpt, it.r);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_all();   // the rows are written before the CTA (and its shared memory) ends
+                }
             }
             if (row_ok) {
                 if (bad) {
@@ -672,9 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // every role is done: the MMA issuer's lanes arrive one by one (its idle
+    // lanes early, the issuing lane once the last MMA has completed), then the
+    // allocating warp, converged again, releases the TMEM
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::block_bar_sync_threads();
     if (warp == kMmaWarp) {
+        __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
@@ -697,7 +751,7 @@ cudaError_t launch_pk_d(const CtxArgs &a, int bpt, int tiles, int sm_count, cuda
         }
     }
     const Geometry &g = a.g;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t qd[4] = {(uint64_t)D, (uint64_t)g.Hq, (uint64_t)g.W_s, (uint64_t)g.R};
     const uint64_t qs[3] = {(uint64_t)D * 2, (uint64_t)g.Hq * D * 2, (uint64_t)g.W_s * g.Hq * D * 2};
     const uint32_t qb[4] = {64, (uint32_t)g.G, (uint32_t)bpt, 1};
@@ -706,7 +760,7 @@ cudaError_t launch_pk_d(const CtxArgs &a, int bpt, int tiles, int sm_count, cuda
     const uint64_t kd[4] = {(uint64_t)D, rows, (uint64_t)g.Hkv, outer};
     const uint64_t ks[3] = {(uint64_t)D * 2, rows * D * 2, (uint64_t)g.Hkv * rows * D * 2};
     const uint32_t kb[4] = {64, (uint32_t)kBN, 1, 1};
-    if (!encode_4d(&tq, a.q, qd, qs, qb)) return cudaErrorInvalidValue;
+    if (!encode_4d(&tq, a.q, qd, qs, qb) || !encode_4d(&to, a.out, qd, qs, qb)) return cudaErrorInvalidValue;
     if (g.Lc_max > 0) {
         if (!encode_4d(&tk, a.ctx_k, kd, ks, kb) || !encode_4d(&tv, a.ctx_v, kd, ks, kb)) return cudaErrorInvalidValue;
     } else {
@@ -719,7 +773,7 @@ cudaError_t launch_pk_d(const CtxArgs &a, int bpt, int tiles, int sm_count, cuda
     p.tiles = tiles;
     p.items = g.R * g.Hkv * tiles;
     const int grid = p.items < sm_count ? p.items : sm_count;
-    ctx_pk_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, p);
+    ctx_pk_kernel<D><<<grid, kThreads, C::kSmem, s>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 

@@ -931,9 +931,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // every role is done: the MMA issuer's lanes arrive one by one (its idle
+    // lanes early, the issuing lane once the last MMA has completed), then the
+    // allocating warp, converged again, releases the TMEM
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::block_bar_sync_threads();
     if (warp == kMmaWarp) {
+        __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }

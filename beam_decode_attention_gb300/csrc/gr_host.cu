@@ -392,7 +392,7 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     auto mark = [&](int i) -> int {
-        if (!events) return GR_OK;
+        if (!events || !events[i]) return GR_OK;
         return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s));
     };
     char *ws = static_cast<char *>(workspace);

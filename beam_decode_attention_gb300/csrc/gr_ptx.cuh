@@ -108,6 +108,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Block-wide barrier 0 that counts threads one by one (the non-aligned form):
+// the lanes of a warp may arrive at different times, as the MMA issuer's idle
+// lanes do while its one issuing lane works.  __syncthreads() is the aligned
+// form, which expects a converged warp.
+__device__ __forceinline__ void block_bar_sync_threads() {
+    asm volatile("barrier.sync 0;" ::: "memory");
+}
+
 // generic-proxy shared-memory writes -> visible to the async proxy (tensor core)
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -689,8 +689,14 @@ def attention_run(gr, torch, spec, steps, warmup, soak_s=0.0, clocks=None):
     if gr.gr_get_device_error() != 0:
         raise RuntimeError(f"device error during the warm-up of {spec.name}")
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(S)]
-              for _ in range(steps)]
+    # events[k][s] = [before the call, after the context kernel, after the
+    # call]; the middle one only when a second kernel follows (each event
+    # record adds about 2 us of device time between its neighbours, so a
+    # one-kernel call is bracketed by two events and its kernel time is the
+    # call time)
+    one_kernel = [p["kernels"] == 1 for p in plans]
+    events = [[[torch.cuda.Event(enable_timing=True), None if one_kernel[s] else torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)] for s in range(S)] for _ in range(steps)]
     if clocks is not None:
         clocks.start()
         time.sleep(0.3)
@@ -713,8 +719,8 @@ def attention_run(gr, torch, spec, steps, warmup, soak_s=0.0, clocks=None):
 
     call_us = np.array([[1000.0 * events[k][s][0].elapsed_time(events[k][s][2]) for s in range(S)]
                         for k in range(steps)])
-    ctx_us = np.array([[1000.0 * events[k][s][0].elapsed_time(events[k][s][1]) for s in range(S)]
-                       for k in range(steps)])
+    ctx_us = np.array([[1000.0 * events[k][s][0].elapsed_time(events[k][s][2 if one_kernel[s] else 1])
+                        for s in range(S)] for k in range(steps)])
     per_step_us = call_us.mean(axis=0)
     per_step_ctx_us = ctx_us.mean(axis=0)
     pk = peaks()
