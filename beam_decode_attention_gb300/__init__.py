@@ -278,9 +278,9 @@ def gr_decode_attn_paged(shape: Shape, pages: CtxPages, q, ctx_k_pool, ctx_v_poo
 def gr_decode_attn_timed(shape: Shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path,
                          widths: Sequence[int], step: int, out, lse, workspace, events,
                          workspace_bytes: Optional[int] = None, stream=None) -> None:
-    """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``
-    or None, which is not recorded) before the context kernel, after it, and
-    after the last kernel."""
+    """gr_decode_attn recording ``events`` (3 ``torch.cuda.Event(enable_timing=True)``;
+    the middle one may be None, and is then not recorded) before the context
+    kernel, after it, and after the last kernel."""
     w = _widths_arr(widths, step)
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -518,7 +518,7 @@ int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *
                          const void *beam_v, const int32_t *beam_path, const int32_t *widths,
                          int32_t step, void *out, float *lse, void *workspace,
                          size_t workspace_bytes, gr_stream_t stream, gr_event_t const *events) {
-    if (!events || !events[0] || !events[1] || !events[2]) return GR_ERR_NULL_ARG;
+    if (!events || !events[0] || !events[2]) return GR_ERR_NULL_ARG;   // events[1] may be NULL
     return run_decode(shape, q, ctx_k, ctx_v, ctx_len, beam_k, beam_v, beam_path, widths, step, out,
                       lse, workspace, workspace_bytes, stream, events);
 }

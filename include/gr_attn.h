@@ -206,11 +206,11 @@ int gr_decode_attn_noalloc(const gr_attn_shape *shape, const void *q, const void
  * before the context-stage kernel, events[1] after it (before the per-beam
  * stage and merge), events[2] after the last kernel.  Elapsed times between
  * them give each kernel's device time without a profiler.  `events` is a
- * HOST array of 3 created events (cudaEventCreate); an entry may be NULL, and
- * that event is then not recorded (on GB300 each record adds about 2 us of
+ * HOST array of 3 created events (cudaEventCreate), of which events[1] may
+ * be NULL and is then not recorded (on GB300 each record adds about 2 us of
  * device time between its neighbours, so a caller timing a call that runs one
- * kernel leaves events[1] NULL).  All other arguments and errors are those of
- * gr_decode_attn.
+ * kernel leaves it NULL); GR_ERR_NULL_ARG when events, events[0] or events[2]
+ * is NULL.  All other arguments and errors are those of gr_decode_attn.
  */
 int gr_decode_attn_timed(const gr_attn_shape *shape, const void *q, const void *ctx_k,
                          const void *ctx_v, const int32_t *ctx_len, const void *beam_k,

@@ -332,12 +332,13 @@ def test_repeatable_and_stream():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("splits", [1, 2])
-def test_bad_parent_is_reported_not_followed(splits):
+@pytest.mark.parametrize("splits,path", [(1, "pair"), (1, "persistent"), (2, "pair")])
+def test_bad_parent_is_reported_not_followed(splits, path):
     """A parent outside [0, W_{t-1}) is counted by gr_validate_beam_path; the
     decode call reads nothing out of range, writes NaN to the rows whose
     chain meets it, flags the device error word, and leaves the other rows
-    right -- in the fused single-split epilogue and in the split path."""
+    right -- in the fused single-split epilogue of both kernels and in the
+    split path."""
     import beam_decode_attention_gb300 as gr
     inp = workloads.make_custom(2, 4, 2, 64, [150, 300], [3, 4, 5], seed=83)
     inp["beam_path"][1, 2, 2] = 4            # widths[1] == 4: out of range
@@ -349,12 +350,16 @@ def test_bad_parent_is_reported_not_followed(splits):
     torch.cuda.synchronize()
     assert int(bad.item()) == 2
     os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    if path == "persistent":
+        os.environ["GR_ATTN_FORCE_PATH"] = "persistent"
     try:
         plan = gr.gr_decode_attn_plan(dev.shape, dev.widths, 2)
         assert plan["fused_merge"] == 1 and plan["kernels"] == 1 and plan["n_splits"] == splits
+        assert plan["persistent"] == (1 if path == "persistent" else 0)
         out, lse = dev.run(2)
     finally:
         os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
     assert gr.gr_get_device_error() == -8    # GR_ERR_BAD_BEAM_PATH
     assert gr.gr_get_device_error() == 0     # reading clears the word
 
