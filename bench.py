@@ -745,6 +745,7 @@ def attention_run(gr, torch, spec, steps, warmup, soak_s=0.0, clocks=None):
         per_step_ctx_us=[round(float(x), 2) for x in per_step_ctx_us],
         tflops=round(total_flops / (per_step_us.sum() * 1e-6) / 1e12, 2),
         ctx_tflops=round(achieved_tf, 2),
+        ctx_gbs=round(sum(w["bytes"] for w in works) / (per_step_ctx_us.sum() * 1e-6) / 1e9, 1),
         roofline_us=[round(x, 2) for x in roof_us], bound=bound,
         call_frac_per_step=[round(a / b, 4) for a, b in zip(roof_us, per_step_us)],
         call_frac=round(sum(roof_us) / float(per_step_us.sum()), 4),
@@ -780,11 +781,20 @@ def main():
     pk = peaks()
     clocks = ClockSampler()
     res = attention_run(gr, torch, spec, args.steps, args.warmup, soak_s=args.clock_soak, clocks=clocks)
-    traffic = recorded_traffic(spec.name)
-    roofline = {"bound": "tensor", "achieved": res["ctx_tflops"], "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": res["ctx_frac_of_bf16"],
-                "traffic": traffic, "kernel": "ctx_tc_kernel (context stage, fused per-beam stage and merge)",
-                "peak_source": f"{pk['source']} bf16 burst"}
+    # the dominant kernel is the one of the slowest decode step
+    slowest = int(np.argmax(res["per_step_us"]))
+    persistent = bool(res["plans"][slowest].get("persistent"))
+    kname = ("ctx_pk_kernel (persistent; context stage, fused per-beam stage and merge)" if persistent else
+             "ctx_tc_kernel (context stage, fused per-beam stage and merge)")
+    traffic = recorded_traffic(spec.name, PK_KERNEL_SOURCES if persistent else None)
+    if res["bound"][slowest] == "hbm":
+        roofline = {"bound": "hbm", "achieved": res["ctx_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(res["ctx_gbs"] / pk["hbm_gbs"], 4), "traffic": traffic, "kernel": kname,
+                    "peak_source": f"{pk['source']} HBM copy"}
+    else:
+        roofline = {"bound": "tensor", "achieved": res["ctx_tflops"], "peak": pk["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": res["ctx_frac_of_bf16"], "traffic": traffic, "kernel": kname,
+                    "peak_source": f"{pk['source']} bf16 burst"}
     call_roofline = {"roofline_us_per_step": res["roofline_us"], "measured_us_per_step": res["per_step_us"],
                      "bound_per_step": res["bound"], "frac_per_step": res["call_frac_per_step"],
                      "frac": res["call_frac"]}
