@@ -427,6 +427,36 @@ __device__ __forceinline__ void merge_tile(const CtxArgs &a, const CUtensorMap *
     }
 }
 
+// Requests ranked by context length, longest first (ties by index): the grid's
+// y index counts (rank, kv head), so the CTAs of the longest requests are
+// dispatched first and the short ones fill the tail of the last wave (a
+// longest-processing-time order; it matters when context lengths differ).
+// Each warp ranks the requests on its own, lane c taking request c, so no
+// block barrier is needed.  Past 32 requests the order stays by index.
+constexpr int kMaxRankedRequests = 32;
+
+__device__ __forceinline__ int request_at_rank(const CtxArgs &a, int rank) {
+    const Geometry &g = a.g;
+    if (g.R <= 1 || g.R > kMaxRankedRequests) return rank;
+    auto blocks = [&](int r) {
+        int len = a.ctx_len[r];
+        len = len < 0 ? 0 : (len > g.Lc_max ? g.Lc_max : len);
+        return (len + tc::kBN - 1) / tc::kBN;
+    };
+    const int c = threadIdx.x & 31;
+    int rk = -1;
+    if (c < g.R) {
+        const int bc = blocks(c);
+        rk = 0;
+        for (int o = 0; o < g.R; ++o) {
+            const int bo = blocks(o);
+            rk += (bo > bc || (bo == bc && o < c)) ? 1 : 0;
+        }
+    }
+    const unsigned m = __ballot_sync(kFullMask, rk == rank);
+    return m ? __ffs(m) - 1 : rank;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -444,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Geometry &g = p.a.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pair = blockIdx.x;
-    const int kvh = blockIdx.y % g.Hkv, r = blockIdx.y / g.Hkv, sp = blockIdx.z;
+    const int kvh = blockIdx.y % g.Hkv, r = request_at_rank(p.a, blockIdx.y / g.Hkv), sp = blockIdx.z;
     const int tile0 = 2 * pair;
     const bool t1_active = (tile0 + 1) < p.tiles;
     const int rows_per_tile = p.bpt * g.G;
