@@ -112,6 +112,24 @@ def test_multi_tile_ragged():
     _run_custom(inp)
 
 
+@pytest.mark.parametrize("R", [31, 33])
+def test_requests_ranked_by_context_length(R):
+    """The tile-pair kernel takes the CTAs of the longest contexts first: the
+    grid's request index is a rank by key blocks (ties by request index),
+    computed in every warp for up to 32 requests and left as the index past
+    that.  Ragged lengths with ties, empty contexts and a long one, on both
+    sides of the 32-request limit: every row still lands in its own place."""
+    rng = np.random.default_rng(500 + R)
+    lens = [int(x) for x in rng.choice([0, 1, 128, 129, 300, 300, 700], size=R)]
+    lens[R // 2] = 1500
+    inp = workloads.make_custom(R, 4, 2, 64, lens, [3, 70, 140], seed=R)
+    os.environ["GR_ATTN_FORCE_PATH"] = "pair"
+    try:
+        _run_custom(inp, splits=1)
+    finally:
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
+
+
 @pytest.mark.parametrize("lens", [[0, 0], [1, 7], [127, 128], [129, 255], [0, 256]])
 def test_context_length_edges(lens):
     inp = workloads.make_custom(2, 16, 8, 128, lens, [3, 9, 65], seed=sum(lens) + 3, lc_max=300)
