@@ -259,11 +259,98 @@ __device__ __forceinline__ void bitonic_desc_shfl(unsigned long long *a, int n) 
     __syncthreads();
 }
 
+// The same descending bitonic sort with EPT consecutive elements per thread
+// (thread t holds elements t * EPT .. t * EPT + EPT - 1, threads t < n / EPT):
+// the strides below EPT are compare-exchanges inside a thread, those below
+// 32 * EPT warp shuffles with lane t ^ (stride / EPT), and only the larger
+// ones (n > 32 * EPT) go through shared memory and a block barrier, where
+// element e of thread t sits at a[e * T + t] (T = n / EPT) so that a warp's
+// accesses fall on consecutive words.  All threads of the block call it; n
+// is a power of two with 32 * EPT <= n <= EPT * blockDim.
+template <int EPT>
+__device__ __forceinline__ void bitonic_desc_blocked(unsigned long long *a, int n) {
+    const int t = threadIdx.x, lane = t & 31, T = n / EPT;
+    const bool active = t < T;   // whole warps (T is a multiple of 32)
+    unsigned long long x[EPT];
+    if (active) {
+        const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(a + t * EPT);
+#pragma unroll
+        for (int q = 0; q < EPT / 2; ++q) {
+            const ulonglong2 v = src[q];
+            x[2 * q] = v.x;
+            x[2 * q + 1] = v.y;
+        }
+    }
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j >= EPT; j >>= 1) {
+            const int m = j / EPT;   // partner thread t ^ m
+            if (m < 32) {
+                if (active) {
+                    const bool lower = (lane & m) == 0;
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) {
+                        const unsigned long long o = shfl_xor_u64(x[e], m);
+                        const bool take_max = (((t * EPT + e) & k) == 0) == lower;
+                        x[e] = take_max ? (o > x[e] ? o : x[e]) : (o < x[e] ? o : x[e]);
+                    }
+                }
+            } else {
+                __syncthreads();   // the previous exchange's reads (and the initial loads) are done
+                if (active) {
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) a[e * T + t] = x[e];
+                }
+                __syncthreads();
+                if (active) {
+                    const bool lower = (t & m) == 0;
+#pragma unroll
+                    for (int e = 0; e < EPT; ++e) {
+                        const unsigned long long o = a[e * T + (t ^ m)];
+                        const bool take_max = (((t * EPT + e) & k) == 0) == lower;
+                        x[e] = take_max ? (o > x[e] ? o : x[e]) : (o < x[e] ? o : x[e]);
+                    }
+                }
+            }
+        }
+        // the strides below EPT, inside each thread (compile-time indices)
+        if (active) {
+#pragma unroll
+            for (int jj = EPT / 2; jj > 0; jj >>= 1) {
+                if (jj >= k) continue;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    if ((e ^ jj) <= e) continue;
+                    const bool desc = ((t * EPT + e) & k) == 0;
+                    const unsigned long long lo = x[e], hi = x[e ^ jj];
+                    const bool sw = desc ? lo < hi : lo > hi;
+                    x[e] = sw ? hi : lo;
+                    x[e ^ jj] = sw ? lo : hi;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (active) {
+        ulonglong2 *dst = reinterpret_cast<ulonglong2 *>(a + t * EPT);
+#pragma unroll
+        for (int q = 0; q < EPT / 2; ++q) dst[q] = make_ulonglong2(x[2 * q], x[2 * q + 1]);
+    }
+    __syncthreads();
+}
+
 // Descending sort of n (a power of two) values: in registers where the
-// shuffle form takes n, else the shared-memory network.
+// shuffle form takes n, else the shared-memory network.  (The row kernels,
+// several CTAs per SM, measured faster with this form; the one-CTA merge
+// with the blocked form below.)
 __device__ __forceinline__ void sort_desc(unsigned long long *a, int n) {
     if (n >= 64 && n <= 4 * (int)blockDim.x) bitonic_desc_shfl(a, n);
     else bitonic_desc(a, n);
+}
+
+// The same with four consecutive elements per thread where n allows.
+__device__ __forceinline__ void sort_desc_blocked(unsigned long long *a, int n) {
+    if (n >= 128 && n <= 4 * (int)blockDim.x) bitonic_desc_blocked<4>(a, n);
+    else sort_desc(a, n);
 }
 
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t low) {
@@ -689,6 +776,12 @@ struct MergeSelArgs {
     const int32_t *beam_node, *trie_offsets, *trie_tokens, *trie_children;
     int32_t *next_node;
     int num_nodes, num_edges;
+    // a list entry's low word is ~u, and its flat index b * flat_mul + u orders
+    // equal scores: u = v (flat_mul = V), or, for item-constrained rows, the
+    // edge index (flat_mul = num_edges; edges are sorted by token within a
+    // node, so the order is the same), which also names the child node
+    unsigned flat_mul;
+    int edge_coded;
 };
 
 // dynamic shared memory of the merge kernel: list offsets, per-list counts
@@ -829,10 +922,15 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
             if (j < n_sel) {
                 const unsigned long long e = src[j];
                 const uint32_t flat = ~(uint32_t)e;
-                pb = (int32_t)(flat / (uint32_t)a.V);
-                tv = (int32_t)(flat % (uint32_t)a.V);
+                pb = (int32_t)(flat / a.flat_mul);
+                const uint32_t u = flat % a.flat_mul;
                 sc = key_float((uint32_t)(e >> 32));
-                if (a.next_node) {
+                tv = (int32_t)u;
+                if (a.edge_coded) {
+                    // the edge itself: its token and child node
+                    tv = a.trie_tokens[u];
+                    if (a.next_node) nd = a.trie_children[u];
+                } else if (a.next_node) {
                     // the edge of the parent's node that carries the token; the node
                     // and its edge range are checked as the rows kernel checks them,
                     // and a search that lands past the range or on another token (a
@@ -860,29 +958,33 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     };
     if (total <= kEntCap) {
         // Every candidate at or above the bound fits in shared memory: read each
-        // once as (score key, ~flat index), find the n_sel-th largest key tau,
-        // keep the entries at or above it and sort them; the first n_sel are
-        // the selection (ties at tau in flat-index order, as the sort puts them).
+        // once as (score key, ~flat index) and sort them in registers (up to
+        // kMaxSel of them; past that only those at or above the n_sel-th
+        // largest key); the first n_sel are the selection, ties in flat-index
+        // order.
         for (int e = threadIdx.x; e < total; e += blockDim.x) {
             int b, j;
             locate(e, b, j);
             const unsigned long long v = lists[(long long)b * a.L + j];
-            const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)v;
+            const uint32_t flat = (uint32_t)b * a.flat_mul + ~(uint32_t)v;
             ent[e] = ((v >> 32) << 32) | (uint32_t)~flat;
         }
         __syncthreads();
         const int n_sel = min(a.next_width, total);
-        int kept = 0;
-        if (n_sel > 0) {
+        int n = total;
+        if (n > kMaxSel && n_sel > 0) {
+            // more than a sort takes cheaply: the n_sel-th largest key first, and
+            // only the entries at or above it (ties included) are sorted
             const uint32_t tau = radix_kth(ent, total, n_sel, hist, red, &s_bin, &s_above);
-            kept = compact(ent, total, red, [&](unsigned long long e) { return (uint32_t)(e >> 32) >= tau; },
-                           [](unsigned long long e) { return e; });
+            n = compact(ent, total, red, [&](unsigned long long e) { return (uint32_t)(e >> 32) >= tau; },
+                        [](unsigned long long e) { return e; });
         }
         int np2 = 1;
-        while (np2 < kept) np2 <<= 1;
-        for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) ent[i] = 0ull;
+        while (np2 < n) np2 <<= 1;
+        for (int i = n + threadIdx.x; i < np2; i += blockDim.x) ent[i] = 0ull;
         __syncthreads();
-        sort_desc(ent, np2);
+        // sorted by (score desc, flat asc): the first n_sel are the selection
+        sort_desc_blocked(ent, np2);
         emit(ent, n_sel);
         return;
     }
@@ -964,7 +1066,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         const int oe = eqc[b], q = eqc[b + 1] - oe;
         if (j >= g + q) continue;
         const unsigned long long ent = lists[(long long)b * a.L + j];
-        const uint32_t flat = (uint32_t)b * (uint32_t)a.V + ~(uint32_t)ent;
+        const uint32_t flat = (uint32_t)b * a.flat_mul + ~(uint32_t)ent;
         const unsigned long long item = ((ent >> 32) << 32) | (uint32_t)~flat;
         if (j < g) sel[og + j] = item;
         else if (oe + (j - g) < need) sel[n_gt + oe + (j - g)] = item;
@@ -974,7 +1076,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     while (np2 < a.next_width) np2 <<= 1;
     for (int i = n_sel + threadIdx.x; i < np2; i += blockDim.x) sel[i] = 0ull;
     __syncthreads();
-    sort_desc(sel, np2);
+    sort_desc_blocked(sel, np2);
     emit(sel, n_sel);
 }
 
@@ -1001,6 +1103,7 @@ struct TrieRowArgs {
     int *big_count;              // rows whose node has more edges than a warp holds
     int *big_rows;               // [R * W_s] those rows, in any order
     int rows, W, V, next_width, num_nodes, num_edges;
+    int edge_coded;              // list entries carry the edge index instead of the token
 };
 
 // A row's trie node and its edge range [p0, p1) (empty for a node index or
@@ -1064,7 +1167,10 @@ __global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(Trie
     // a skipped edge sorts last and is not kept: key 0 is below every score
     unsigned long long e[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) e[j] = v[j] >= 0 ? pack(ord_key(score_of(x[j], c, S)), ~(uint32_t)v[j]) : 0ull;
+    for (int j = 0; j < 8; ++j)
+        e[j] = v[j] >= 0 ? pack(ord_key(score_of(x[j], c, S)),
+                                ~(uint32_t)(a.edge_coded ? p0 + 8 * lane + j : v[j]))
+                         : 0ull;
     // descending bitonic sort of the warp's 256 elements (index i = 8 * lane + j)
 #pragma unroll
     for (int k = 2; k <= kTrieWarpDeg; k <<= 1) {
@@ -1173,7 +1279,9 @@ __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) 
         for (int k = threadIdx.x; k < m; k += blockDim.x) {
             int v;
             // a skipped edge sorts last and is not kept: key 0 is below every score
-            buf[cnt + k] = legal(base + k, v) ? pack(ord_key(score_of(__ldg(z + v), c, S)), ~(uint32_t)v) : 0ull;
+            buf[cnt + k] = legal(base + k, v) ? pack(ord_key(score_of(__ldg(z + v), c, S)),
+                                                     ~(uint32_t)(a.edge_coded ? p0 + base + k : v))
+                                              : 0ull;
         }
         const int tot = cnt + m;
         int np2 = 1;
@@ -1281,6 +1389,8 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ma.parent_stride = parent_stride;
     ma.next_token = next_token;
     ma.next_score = next_score;
+    ma.flat_mul = (unsigned)V;
+    ma.edge_coded = 0;
     select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
     return cudaGetLastError();
 }
@@ -1341,6 +1451,8 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ta.num_edges = num_edges;
     ta.big_count = big_count;
     ta.big_rows = big_rows;
+    // edge-coded entries while every flat index b * num_edges + e fits 32 bits
+    ta.edge_coded = (num_edges > 0 && (unsigned long long)W * (unsigned long long)num_edges < (1ull << 32)) ? 1 : 0;
     trie_rows_warp_kernel<<<(R * W + kTrieWarpRows - 1) / kTrieWarpRows, kTrieWarpRows * 32, 0, s>>>(ta);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1370,6 +1482,8 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ma.next_node = next_node;
     ma.num_nodes = num_nodes;
     ma.num_edges = num_edges;
+    ma.edge_coded = ta.edge_coded;
+    ma.flat_mul = ta.edge_coded ? (unsigned)num_edges : (unsigned)V;
     select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
     return cudaGetLastError();
 }
