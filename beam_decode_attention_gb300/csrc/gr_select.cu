@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     const int b0 = min(a.W, (int)threadIdx.x * per), b1 = min(a.W, b0 + per);
     // A tighter bound: the next_width-th largest key among the first kh keys
     // of every list (real candidates, so at least next_width entries reach it).
-    const int kh = min(32, max(1, (4 * a.next_width + a.W - 1) / a.W));
+    const int kh = min(32, max(1, (8 * a.next_width + a.W - 1) / a.W));
     // the keys go where offs, gtc and eqc will be (not yet in use)
     const unsigned *heads = reinterpret_cast<const unsigned *>(offs);
     const bool have_heads = a.W * kh <= 3 * (kMaxBeams + 1);
