@@ -14,7 +14,8 @@
 //
 // Work item = (request, kv head, 128-row tile); the grid holds at most one
 // CTA per SM and each CTA walks the items blockIdx.x, + gridDim.x, ...
-// Consecutive items and key blocks overlap:
+// Consecutive key blocks overlap, and so do consecutive items up to their O
+// (the next item's loads and S run while the epilogue drains the last one):
 //   TMEM    S_0 [0,128) S_1 [128,256): S of consecutive key blocks (global
 //           block n uses S_{n&1}), so S(n+1) is computed while the softmax
 //           of block n runs; O [256,256+D): the item's context partial;
@@ -33,7 +34,8 @@
 //               accumulates their V rows into C (a softmax of its own, with
 //               the chain's maximum and sum kept in registers); once O is
 //               complete, merges the two partials by log-sum-exp from TMEM
-//               and writes the bf16 row and its LSE.
+//               and writes the bf16 row (the CTA's last item through its
+//               freed Q tile and a TMA store) and its LSE.
 //   warp 8      TMA producer of the Q tiles and the K ring.
 //   warp 9      MMA issuer (one lane).
 //   warp 10     TMA producer of the V ring (zeroes V rows past ctx_len).

@@ -357,6 +357,13 @@ __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t low) {
     return ((unsigned long long)key << 32) | low;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the one ahead of it has finished, and
+// waits here until that grid has completed and its writes are visible (a
+// no-op when launched without it); a kernel lets the next one start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Keeps the entries e of a[0, n) with keep(e), transformed by xf(e), at the
 // front of a, in their order (chunk by chunk, a block-wide scan each);
 // returns the count (every thread).
@@ -799,6 +806,7 @@ constexpr int kMergeSmem = (3 * (kMaxBeams + 1) + kHistBins) * 4 + (kMaxSel + kE
 // order (lists in b order, each list in v order: the lists are sorted), and
 // the W' are sorted by (score desc, flat asc).
 __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSelArgs a) {
+    grid_dep_wait();   // the row lists, lengths and bounds of the kernel(s) before
     extern __shared__ unsigned long long msm[];
     unsigned long long *sel = msm;                           // [kMaxSel] (8-byte entries first)
     unsigned long long *ent = sel + kMaxSel;                 // [kEntCap] the candidates at or above the bound
@@ -1131,6 +1139,9 @@ constexpr int kTrieWarpDeg = 256;
 constexpr int kTrieWarpRows = 8;   // rows (warps) per CTA
 
 __global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(TrieRowArgs a) {
+    // the wide-row kernel may be scheduled now (it waits for this grid): every
+    // CTA of this grid is resident at once, so it takes no slot from them
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kTrieWarpRows + (threadIdx.x >> 5);
     if (row >= a.rows) return;   // warp-uniform
@@ -1230,6 +1241,8 @@ __global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(Trie
 // The rows whose node has more edges than a warp holds, one CTA at a time per
 // row (grid-strided over big_rows).
 __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) {
+    grid_dep_wait();   // the wide-row list of the warp kernel
+    grid_dep_launch();
     __shared__ unsigned long long buf[kMaxSel + kTrieChunk];
     __shared__ MaxSum s_ms[kTrieThreads / 32];
     __shared__ float s_c;
@@ -1317,6 +1330,27 @@ __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) 
 static size_t list_bytes(int R, int W, int L) { return (size_t)R * W * L * sizeof(unsigned long long); }
 static size_t bound_bytes(int R) { return ((size_t)R * 4 + 15) / 16 * 16; }
 
+// Launches a kernel that may start while the one before it on the stream
+// finishes (programmatic stream serialization; the kernel waits in
+// grid_dep_wait before reading that kernel's output).  Without `overlap`
+// it is an ordinary launch (an event recorded between the two kernels must
+// see the first one complete).
+template <typename... Params, typename... Args>
+static cudaError_t launch_after(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                bool overlap, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 size_t select_list_bytes(int R, int W, int V, int next_width) {
     const int L = next_width < V ? next_width : V;
     return list_bytes(R, W, L) + bound_bytes(R) + (size_t)R * W * sizeof(int);
@@ -1391,7 +1425,8 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ma.next_score = next_score;
     ma.flat_mul = (unsigned)V;
     ma.edge_coded = 0;
-    select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
+    e = launch_after(select_merge_kernel, dim3(R), dim3(kMergeThreads), kMergeSmem, s, between == nullptr, ma);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -1458,7 +1493,8 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     if (e != cudaSuccess) return e;
     {
         const int grid = R * W < 2 * sm_count[dev] ? R * W : 2 * sm_count[dev];
-        trie_rows_kernel<<<grid, kTrieThreads, 0, s>>>(ta);
+        e = launch_after(trie_rows_kernel, dim3(grid), dim3(kTrieThreads), 0, s, true, ta);
+        if (e != cudaSuccess) return e;
     }
     e = cudaGetLastError();
     if (e == cudaSuccess && between) e = cudaEventRecord(between, s);
@@ -1484,7 +1520,8 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ma.num_edges = num_edges;
     ma.edge_coded = ta.edge_coded;
     ma.flat_mul = ta.edge_coded ? (unsigned)num_edges : (unsigned)V;
-    select_merge_kernel<<<R, kMergeThreads, kMergeSmem, s>>>(ma);
+    e = launch_after(select_merge_kernel, dim3(R), dim3(kMergeThreads), kMergeSmem, s, between == nullptr, ma);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

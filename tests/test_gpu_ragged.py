@@ -56,11 +56,13 @@ def run_ragged(dev, W, step):
     return o, lse.cpu().numpy().reshape(R, Wp, Hq)
 
 
-@pytest.mark.parametrize("splits", [1, 2])
-def test_ragged_rows_match_oracle_and_padded_call(splits):
+@pytest.mark.parametrize("splits,path", [(1, "pair"), (1, "persistent"), (2, "pair")])
+def test_ragged_rows_match_oracle_and_padded_call(splits, path):
     inp, W = ragged_inputs(WIDTHS, seed=91 + splits)
     dev = DeviceWorkload(inp)
     os.environ["GR_ATTN_FORCE_SPLITS"] = str(splits)
+    if path == "persistent":
+        os.environ["GR_ATTN_FORCE_PATH"] = "persistent"
     try:
         for step in range(3):
             assert gr.gr_get_device_error() == 0
@@ -75,6 +77,7 @@ def test_ragged_rows_match_oracle_and_padded_call(splits):
                 assert np.array_equal(lse[r, :w], dense_lse[r, :w], equal_nan=True)
     finally:
         os.environ.pop("GR_ATTN_FORCE_SPLITS", None)
+        os.environ.pop("GR_ATTN_FORCE_PATH", None)
 
 
 def test_ragged_parent_checked_against_request_width():
