@@ -266,9 +266,10 @@ __device__ __forceinline__ void bitonic_desc_shfl(unsigned long long *a, int n) 
 // ones (n > 32 * EPT) go through shared memory and a block barrier, where
 // element e of thread t sits at a[e * T + t] (T = n / EPT) so that a warp's
 // accesses fall on consecutive words.  All threads of the block call it; n
-// is a power of two with 32 * EPT <= n <= EPT * blockDim.
+// is a power of two with 32 * EPT <= n <= EPT * blockDim.  Not inlined: in
+// the row kernel (64 registers a thread) inlining it cost spills elsewhere.
 template <int EPT>
-__device__ __forceinline__ void bitonic_desc_blocked(unsigned long long *a, int n) {
+__device__ __noinline__ void bitonic_desc_blocked(unsigned long long *a, int n) {
     const int t = threadIdx.x, lane = t & 31, T = n / EPT;
     const bool active = t < T;   // whole warps (T is a multiple of 32)
     unsigned long long x[EPT];
@@ -339,9 +340,7 @@ __device__ __forceinline__ void bitonic_desc_blocked(unsigned long long *a, int 
 }
 
 // Descending sort of n (a power of two) values: in registers where the
-// shuffle form takes n, else the shared-memory network.  (The row kernels,
-// several CTAs per SM, measured faster with this form; the one-CTA merge
-// with the blocked form below.)
+// shuffle form takes n, else the shared-memory network.
 __device__ __forceinline__ void sort_desc(unsigned long long *a, int n) {
     if (n >= 64 && n <= 4 * (int)blockDim.x) bitonic_desc_shfl(a, n);
     else bitonic_desc(a, n);
@@ -383,8 +382,12 @@ __device__ __forceinline__ int compact(unsigned long long *arr, int n, int *red,
     return kept;
 }
 
+__device__ __noinline__ void find_bin_call(const int *hist, int need, int *red, int *s_bin, int *s_above);
+
 // The need-th largest key among cand[0, n) (high 32 bits), by a radix select
-// in shared memory (12 + 12 + 8 bits); every thread gets it.
+// in shared memory (12 + 12 + 8 bits); every thread gets it.  kCalls: the bin
+// searches as calls (the per-row kernel's form, see find_bin_call).
+template <bool kCalls = false>
 __device__ __forceinline__ uint32_t radix_kth(const unsigned long long *cand, int n, int need, int *hist, int *red,
                                               int *s_bin, int *s_above) {
     uint32_t prefix = 0, mask = 0;
@@ -400,13 +403,25 @@ __device__ __forceinline__ uint32_t radix_kth(const unsigned long long *cand, in
             if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
         }
         __syncthreads();
-        find_bin(hist, need, red, s_bin, s_above);
+        if (kCalls) find_bin_call(hist, need, red, s_bin, s_above);
+        else find_bin(hist, need, red, s_bin, s_above);
         need -= *s_above;
         prefix |= (bm - (uint32_t)(kHistBins - 1 - *s_bin)) << sh;
         mask |= bm << sh;
         __syncthreads();
     }
     return prefix;
+}
+
+// Out-of-line copies for the per-row kernel (64 registers a thread): as calls
+// they leave the row's stream its registers, and that kernel measured 5 %
+// faster so; the merge kernel keeps them inlined (it measured slower as calls).
+__device__ __noinline__ void find_bin_call(const int *hist, int need, int *red, int *s_bin, int *s_above) {
+    find_bin(hist, need, red, s_bin, s_above);
+}
+__device__ __noinline__ uint32_t radix_kth_call(const unsigned long long *cand, int n, int need, int *hist, int *red,
+                                               int *s_bin, int *s_above) {
+    return radix_kth<true>(cand, n, need, hist, red, s_bin, s_above);
 }
 
 // The exact candidate set of a row without a usable threshold: the L-th
@@ -432,7 +447,7 @@ __device__ __forceinline__ int exact_candidates(const float *z, int V, int L, fl
             if ((k & mask) == prefix) atomicAdd(&hist[kHistBins - 1 - (int)(bm - ((k >> sh) & bm))], 1);
         });
         __syncthreads();
-        find_bin(hist, need, red, s_bin, s_above);
+        find_bin_call(hist, need, red, s_bin, s_above);
         const uint32_t digit = bm - (uint32_t)(kHistBins - 1 - *s_bin);
         need -= *s_above;
         prefix |= digit << sh;
@@ -553,7 +568,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
             if (threadIdx.x + k * (int)blockDim.x < F) atomicAdd(&hist[ord_key(xf[k]) >> (32 - kHistBits)], 1);
         __syncthreads();
         const int need_s = a.V <= F ? a.L : min(F, 2 * (int)(((long long)F * a.L + a.V - 1) / a.V) + 16);
-        find_bin(hist, need_s, red, &s_bin, &s_above);
+        find_bin_call(hist, need_s, red, &s_bin, &s_above);
         const uint32_t b_hi = (uint32_t)s_bin;
         const int need_lo = need_s - s_above;
         __syncthreads();
@@ -565,7 +580,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
             if (threadIdx.x + k * (int)blockDim.x < F && (key >> 20) == b_hi) atomicAdd(&hist[(key >> 8) & 0xfffu], 1);
         }
         __syncthreads();
-        find_bin(hist, need_lo, red, &s_bin, &s_above);
+        find_bin_call(hist, need_lo, red, &s_bin, &s_above);
         const uint32_t tau_key = (b_hi << 20) | ((uint32_t)s_bin << 8);
         // keys at or below 0x7fffff hold -inf and NaN patterns: no threshold there
         const float tau = tau_key <= 0x7fffffu ? -INFINITY : key_float(tau_key);
@@ -723,7 +738,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
                 cand[i] = pack(ord_key(score_of(key_float((uint32_t)(e >> 32)), c, S)), (uint32_t)e);
             }
             __syncthreads();
-            kl = radix_kth(cand, n, a.L, hist, red, &s_bin, &s_above);
+            kl = radix_kth_call(cand, n, a.L, hist, red, &s_bin, &s_above);
             if (tau != -INFINITY) {
                 const float below = nextafterf(tau, -INFINITY);
                 exact = kl > ord_key(score_of(below, c, S));
@@ -731,7 +746,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         }
         if (!exact) {
             n = exact_candidates(z, a.V, a.L, c, S, cand, hist, red, &s_bin, &s_above, &s_cnt);
-            kl = radix_kth(cand, n, a.L, hist, red, &s_bin, &s_above);
+            kl = radix_kth_call(cand, n, a.L, hist, red, &s_bin, &s_above);
         }
         // Only candidates at or above the larger of kl and the request's
         // published bound can be selected (kl bounds the request's W'-th score
@@ -757,7 +772,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         while (np2 < kept) np2 <<= 1;
         for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
         __syncthreads();
-        sort_desc(cand, np2);
+        sort_desc_blocked(cand, np2);
         const int cnt = min(kept, a.L);
         unsigned long long *out = a.lists + (long long)row * a.L;
         for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = cand[j];
