@@ -95,6 +95,24 @@ def test_node_with_more_edges_than_a_chunk():
     check(inp["logits"], inp["beam_scores"], inp["beam_node"], t["offsets"], t["tokens"], t["children"], 1000, got)
 
 
+def test_entries_keep_the_token_when_edge_indices_overflow():
+    """The list entries carry the edge index while W * num_edges fits 32 bits,
+    and the token otherwise (the merge then finds the child by a search of the
+    parent's node).  4096 beams over 513 nodes of 2048 edges each (1,050,624
+    edges) take the second form, through the wide-row kernel."""
+    W, V, N, n = 4096, 2048, 513, 64
+    assert W * N * V >= 1 << 32
+    rng = np.random.default_rng(513)
+    offsets = (np.arange(N + 1) * V).astype(np.int32)
+    tokens = np.tile(np.arange(V, dtype=np.int32), N)
+    children = rng.integers(0, N, size=N * V).astype(np.int32)
+    logits = rng.standard_normal(size=(1, W, V), dtype=np.float32) * np.float32(2.0)
+    scores = (-np.abs(rng.standard_normal(size=(1, W), dtype=np.float32)) * np.float32(3.0))
+    beam_node = rng.integers(0, N, size=(1, W)).astype(np.int32)
+    got = run(logits, scores, beam_node, offsets, tokens, children, n)
+    check(logits, scores, beam_node, offsets, tokens, children, n, got)
+
+
 def test_rows_wide_and_narrow_in_one_request():
     """Beams at a node with more edges than one warp holds (the block kernel)
     and beams at small nodes (the warp kernel) in the same requests: both
