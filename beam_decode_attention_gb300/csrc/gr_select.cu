@@ -27,9 +27,17 @@
 //   A row whose kept set is not provably complete (a skewed prefix, ties,
 //   peaked or degenerate logits) takes an exact radix select on the scores
 //   over the whole row instead (more passes, same result).
-// Each row also publishes its L-th score key (atomicMax per request): with
-// L = W' that row alone holds W' candidates at or above it, so it bounds the
-// request's W'-th score from below.
+// Each row also publishes lower bounds on its request's W'-th score key
+// (valid when L = W'):
+//   its L-th score key (atomicMax per request): that row alone holds W'
+//                 candidates at or above it;
+//   its k-th score key into slot b mod m of m per-request slots (atomicMax,
+//                 k = ceil(W' / m)): m distinct rows then hold m * k >= W'
+//                 candidates at or above the smallest slot, once every slot
+//                 is set.
+// A row that finds the bound above every score its threshold can have left
+// out keeps the candidates at or above the bound without selecting its own
+// L-th (most rows after each request's first ones).
 // Kernel 2 (select_merge_kernel), one CTA per request: a tighter bound from
 // the first keys of every list; each sorted list's prefix at or above it; the
 // W'-th largest score over those prefixes by a radix select in shared
@@ -50,8 +58,10 @@ constexpr int kRowBlocksPerSm = 4;    // row CTAs resident per SM
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kCap = 4096;            // candidate slots per row in shared memory
+constexpr int kSide = kHistBins / 2;  // 8-byte entries the histogram's space holds
 constexpr int kMergeThreads = 1024;
 constexpr int kMaxSel = 1024;         // GR_SELECT_MAX_WIDTH
+constexpr int kBoundSlots = 32;       // per-request slots of rows' k-th score keys
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 
@@ -78,6 +88,8 @@ struct RowArgs {
     unsigned long long *lists;   // [R * W_s][L] (score key << 32 | ~v), sorted descending
     int *plen;                   // [R * W_s] entries written to each list (<= L)
     unsigned *tau_lb;            // [R] lower bound on each request's W'-th score key (null: none)
+    unsigned *tau_slot;          // [R][nslot] rows' slot_k-th score keys, by beam mod nslot
+    int nslot, slot_k;           // nslot * slot_k >= W'
     int rows, W, V, L;
 };
 
@@ -543,6 +555,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
     __shared__ int s_bin, s_above, s_cnt;
     __shared__ int s_wcnt[kRowWarps];   // candidates of each warp's region
     __shared__ float s_c;
+    __shared__ unsigned s_lb;
     const int warp = threadIdx.x >> 5;
     unsigned long long *wreg = cand + warp * kWarpCap;   // this warp's region
 
@@ -729,15 +742,42 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         }
         if (overflow) n = kCap + 1;
 
-        // 3. score keys, the row's L-th, and whether the set is exact
+        // the request's bound so far: the largest published L-th key, and the
+        // smallest slot once every slot is set (0: none)
+        uint32_t lb = 0u;
+        if (a.tau_lb) {
+            if (warp == 0) {
+                const int lane = threadIdx.x & 31;
+                const int req = row / a.W;
+                uint32_t v = lane < a.nslot ? *reinterpret_cast<volatile unsigned *>(a.tau_slot + req * a.nslot + lane)
+                                            : ~0u;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFullMask, v, o));
+                if (lane == 0) {
+                    const uint32_t l = *reinterpret_cast<volatile unsigned *>(a.tau_lb + req);
+                    s_lb = max(a.nslot > 0 ? v : 0u, l);
+                }
+            }
+            __syncthreads();
+            lb = s_lb;
+        }
+
+        // 3. score keys; the bound settles the row when every logit below the
+        // threshold scores below it (then the kept set holds every candidate
+        // at or above the bound); otherwise the row's L-th, and whether the
+        // set is exact
         uint32_t kl = 0u;
-        bool exact = n >= a.L && n <= kCap;
+        bool settled = lb != 0u && n <= kCap;
+        if (settled && tau != -INFINITY) settled = lb > ord_key(score_of(nextafterf(tau, -INFINITY), c, S));
+        bool exact = settled || (n >= a.L && n <= kCap);
         if (exact) {
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
                 const unsigned long long e = cand[i];
                 cand[i] = pack(ord_key(score_of(key_float((uint32_t)(e >> 32)), c, S)), (uint32_t)e);
             }
             __syncthreads();
+        }
+        if (exact && !settled) {
             kl = radix_kth_call(cand, n, a.L, hist, red, &s_bin, &s_above);
             if (tau != -INFINITY) {
                 const float below = nextafterf(tau, -INFINITY);
@@ -749,36 +789,64 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
             kl = radix_kth_call(cand, n, a.L, hist, red, &s_bin, &s_above);
         }
         // Only candidates at or above the larger of kl and the request's
-        // published bound can be selected (kl bounds the request's W'-th score
-        // from below when L = W'): keep those (the row's best, at most L of
-        // them, plus ties), sort and write them.
-        uint32_t keep = kl;
-        if (a.tau_lb) {
-            const uint32_t lbnow = *reinterpret_cast<volatile unsigned *>(a.tau_lb + row / a.W);
-            keep = lbnow > keep ? lbnow : keep;
-        }
-        int kept = 0;
+        // bound can be selected (kl bounds the request's W'-th score from
+        // below when L = W'): keep those (the row's best, at most L of them,
+        // plus ties), sort and write them.
+        const uint32_t keep = kl > lb ? kl : lb;
+        // The kept entries go to the histogram's space (free from here on) in
+        // any order, one shared atomic per warp and step: the sort below
+        // orders them.  Past its kSide entries the candidate array is
+        // compacted in place instead, by a block scan.
+        unsigned long long *side = reinterpret_cast<unsigned long long *>(hist);
+        if (threadIdx.x == 0) s_cnt = 0;
+        __syncthreads();
         for (int base = 0; base < n; base += blockDim.x) {
             const int i = base + threadIdx.x;
-            const unsigned long long e = i < n ? cand[i] : 0ull;
-            const int f = (i < n && (uint32_t)(e >> 32) >= keep) ? 1 : 0;
-            int tot;
-            const int pos = block_excl_scan(f, red, &tot);   // synchronises before any write below
-            if (f) cand[kept + pos] = e;
-            kept += tot;
-            __syncthreads();
+            const bool f = i < n && (uint32_t)(cand[i] >> 32) >= keep;
+            const unsigned m = __ballot_sync(kFullMask, f);
+            if (m) {
+                const int lane = threadIdx.x & 31;
+                int b0 = 0;
+                if (lane == 0) b0 = atomicAdd(&s_cnt, __popc(m));
+                b0 = __shfl_sync(kFullMask, b0, 0);
+                const int pos = b0 + __popc(m & ((1u << lane) - 1u));
+                if (f && pos < kSide) side[pos] = cand[i];
+            }
+        }
+        __syncthreads();
+        int kept = s_cnt;
+        unsigned long long *srt = side;
+        if (kept > kSide) {
+            srt = cand;
+            kept = 0;
+            for (int base = 0; base < n; base += blockDim.x) {
+                const int i = base + threadIdx.x;
+                const unsigned long long e = i < n ? cand[i] : 0ull;
+                const int f = (i < n && (uint32_t)(e >> 32) >= keep) ? 1 : 0;
+                int tot;
+                const int pos = block_excl_scan(f, red, &tot);   // synchronises before any write below
+                if (f) cand[kept + pos] = e;
+                kept += tot;
+                __syncthreads();
+            }
         }
         int np2 = 1;
         while (np2 < kept) np2 <<= 1;
-        for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) cand[i] = 0ull;
+        for (int i = kept + threadIdx.x; i < np2; i += blockDim.x) srt[i] = 0ull;
         __syncthreads();
-        sort_desc_blocked(cand, np2);
+        sort_desc_blocked(srt, np2);
         const int cnt = min(kept, a.L);
         unsigned long long *out = a.lists + (long long)row * a.L;
-        for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = cand[j];
+        for (int j = threadIdx.x; j < cnt; j += blockDim.x) out[j] = srt[j];
         if (threadIdx.x == 0) {
             a.plen[row] = cnt;
-            if (a.tau_lb) atomicMax(a.tau_lb + row / a.W, kl);
+            if (a.tau_lb) {
+                // the row holds slot_k candidates at or above its slot_k-th
+                const int req = row / a.W, beam = row - req * a.W;
+                if (kept >= a.slot_k)
+                    atomicMax(a.tau_slot + req * a.nslot + beam % a.nslot, (unsigned)(srt[a.slot_k - 1] >> 32));
+                if (keep != 0u) atomicMax(a.tau_lb + req, keep);
+            }
         }
         __syncthreads();
     }
@@ -1340,10 +1408,10 @@ __global__ void __launch_bounds__(kTrieThreads) trie_rows_kernel(TrieRowArgs a) 
 
 }  // namespace
 
-// workspace: row lists [R * W][L] u64 | lower bounds [R] u32 (16-byte padded) |
-// list lengths [R * W] int32
+// workspace: row lists [R * W][L] u64 | lower bounds [R] u32 and bound slots
+// [R][kBoundSlots] u32 (16-byte padded) | list lengths [R * W] int32
 static size_t list_bytes(int R, int W, int L) { return (size_t)R * W * L * sizeof(unsigned long long); }
-static size_t bound_bytes(int R) { return ((size_t)R * 4 + 15) / 16 * 16; }
+static size_t bound_bytes(int R) { return ((size_t)R * (1 + kBoundSlots) * 4 + 15) / 16 * 16; }
 
 // Launches a kernel that may start while the one before it on the stream
 // finishes (programmatic stream serialization; the kernel waits in
@@ -1406,7 +1474,7 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     // the bound is only valid when a row alone holds W' candidates (V >= W')
     const bool bound = L == next_width;
     if (bound) {
-        e = cudaMemsetAsync(tau_lb, 0, (size_t)R * 4, s);
+        e = cudaMemsetAsync(tau_lb, 0, (size_t)R * (1 + kBoundSlots) * 4, s);
         if (e != cudaSuccess) return e;
     }
     RowArgs ra;
@@ -1414,6 +1482,9 @@ cudaError_t launch_beam_select(int R, int W, int V, int next_width, const float 
     ra.beam_scores = beam_scores;
     ra.lists = reinterpret_cast<unsigned long long *>(wsb);
     ra.tau_lb = bound ? tau_lb : nullptr;
+    ra.tau_slot = tau_lb + R;
+    ra.nslot = W < kBoundSlots ? W : kBoundSlots;
+    ra.slot_k = (next_width + ra.nslot - 1) / ra.nslot;
     ra.plen = counts;
     ra.rows = R * W;
     ra.W = W;

@@ -118,8 +118,8 @@ def _sel(**kw):
 
 def _sel_bytes(R, W, V, n):
     # per beam row a sorted list of min(n, V) 8-byte entries and its length;
-    # per request a 4-byte bound (padded to 16 bytes)
-    return R * W * min(n, V) * 8 + (R * 4 + 15) // 16 * 16 + R * W * 4
+    # per request a 4-byte bound and 32 4-byte bound slots (padded to 16 bytes)
+    return R * W * min(n, V) * 8 + (R * 33 * 4 + 15) // 16 * 16 + R * W * 4
 
 
 def test_beam_select_workspace_size(lib):
