@@ -906,7 +906,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     const int per = (a.W + blockDim.x - 1) / blockDim.x;
     const int b0 = min(a.W, (int)threadIdx.x * per), b1 = min(a.W, b0 + per);
     // A tighter bound: the next_width-th largest key among the first kh keys
-    // of every list (real candidates, so at least next_width entries reach it).
+    // of every list (real candidates, so at least next_width entries reach it),
+    // to its top 24 bits: a radix select of two 12-bit passes, the key's low 8
+    // bits left zero (a lower bound still, looser by at most one 256-ulp bin).
     const int kh = min(32, max(1, (8 * a.next_width + a.W - 1) / a.W));
     // the keys go where offs, gtc and eqc will be (not yet in use)
     const unsigned *heads = reinterpret_cast<const unsigned *>(offs);
@@ -926,9 +928,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         if (nh >= a.next_width) {
             uint32_t prefix = 0, mask = 0;
             int need = a.next_width;
-            const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+            const int shifts[2] = {20, 8}, widths[2] = {12, 12};
 #pragma unroll
-            for (int rd = 0; rd < 3; ++rd) {
+            for (int rd = 0; rd < 2; ++rd) {
                 for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
                 __syncthreads();
                 const int sh = shifts[rd];
