@@ -55,6 +55,7 @@ constexpr int kTmemCols = 512;
 // bf16 ranges, so the running maximum may lag the true one by up to 16 (log2)
 constexpr float kSumLimit = 65536.0f;
 constexpr int kFusedMaxTokens = 8;          // chain tokens the fused epilogue holds (steps < 8)
+constexpr int kPrefetchBlocks = 1;          // K/V blocks of the next wave's CTA prefetched into L2
 
 // barrier slots
 constexpr int kBarKvFull = 0;               // [kStages]
@@ -92,6 +93,7 @@ struct TcParams {
     CtxArgs a;
     int bpt;    // beams per tile
     int tiles;  // tiles per (request, kv head)
+    int sms;    // CTAs resident at once (one per SM)
 };
 
 // A tile's fp32 rows in shared memory as a TMA tensor copy lays them out
@@ -558,6 +560,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
+        // The CTA one wave on (linear index + SMs) takes an SM as CTAs of this
+        // wave finish: its Q tiles and first K/V blocks are prefetched into L2
+        // once this CTA's last load is out, so its first S does not wait on
+        // DRAM.
+        const long long total = (long long)gridDim.x * gridDim.y * gridDim.z;
+        const long long succ =
+            (long long)blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z) + p.sms;
+        int s_r = -1, s_kvh = 0, s_tile0 = 0, s_kbeg = 0, s_len = 0;
+        if (p.sms > 0 && succ < total) {   // warp-uniform
+            const int sx = (int)(succ % gridDim.x);
+            const int sy = (int)((succ / gridDim.x) % gridDim.y);
+            const int sz = (int)(succ / ((long long)gridDim.x * gridDim.y));
+            s_r = request_at_rank(p.a, sy / g.Hkv);   // warp-collective
+            s_kvh = sy % g.Hkv;
+            s_tile0 = 2 * sx;
+            s_kbeg = sz * p.a.sp.split_len;
+            int sl = p.a.ctx_len[s_r];
+            sl = sl < 0 ? 0 : (sl > g.Lc_max ? g.Lc_max : sl);
+            s_len = min(s_kbeg + p.a.sp.split_len, sl) - s_kbeg;
+        }
         int issued = 1;   // the Q tiles and load 0 went out before the CTA-wide barrier
         bool ok = true;
         if (nb > 0) {
@@ -604,6 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_warp(bar(kBarQFull), 0, nullptr);
                 for (int n = issued - kStages < 0 ? 0 : issued - kStages; n < issued; ++n)
                     wait_warp(bar(kBarKvFull + n % kStages), (n / kStages) & 1, nullptr);
+            } else if (s_r >= 0 && lane == 0) {
+                const int nt = (s_tile0 + 1 < p.tiles) ? 2 : 1;
+                for (int t = 0; t < nt; ++t)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        ptx::tma_prefetch_4d(&tm_q, h * 64, s_kvh * g.G, (s_tile0 + t) * p.bpt, s_r);
+                for (int b = 0; b < kPrefetchBlocks && b * kBN < s_len; ++b) {
+                    int c1, c3;
+                    kv_coords(p.a, s_r, s_kbeg + b * kBN, c1, c3);
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        ptx::tma_prefetch_4d(&tm_k, h * 64, c1, s_kvh, c3);
+                        ptx::tma_prefetch_4d(&tm_v, h * 64, c1, s_kvh, c3);
+                    }
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -976,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------- host side
 
 template <int D>
-cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
+cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, int sm_count, cudaStream_t s) {
     using C = Cfg<D>;
     static std::mutex mu;
     static bool attr_set[64] = {};
@@ -1009,6 +1044,7 @@ cudaError_t launch_d(const CtxArgs &a, int bpt, int tiles, cudaStream_t s) {
     p.a = a;
     p.bpt = bpt;
     p.tiles = tiles;
+    p.sms = sm_count;
     dim3 grid((tiles + 1) / 2, g.R * g.Hkv, a.sp.n_splits);
     // fused path and split merge: the output rows leave by TMA stores with the
     // Q tiles' geometry
@@ -1065,11 +1101,11 @@ int tc_beams_per_tile(int G) { return kBM / G; }
 int tc_fused_max_steps(int) { return kFusedMaxTokens; }
 int tc_merge_max_splits() { return kMaxMergeSplits; }
 
-cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s) {
+cudaError_t launch_ctx_tc(const CtxArgs &a, int sm_count, cudaStream_t s) {
     const int bpt = tc_beams_per_tile(a.g.G);
     const int tiles = (a.g.W_s + bpt - 1) / bpt;
-    if (a.g.D == 128) return launch_d<128>(a, bpt, tiles, s);
-    return launch_d<64>(a, bpt, tiles, s);
+    if (a.g.D == 128) return launch_d<128>(a, bpt, tiles, sm_count, s);
+    return launch_d<64>(a, bpt, tiles, sm_count, s);
 }
 
 }  // namespace gr

@@ -433,7 +433,7 @@ int run_decode(const gr_attn_shape *shape, const void *q, const void *ctx_k, con
         if (persistent(g, sp))
             rc = cuda_status(launch_ctx_pk(c, dev.sm_count, s));
         else
-            rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, s));
+            rc = cuda_status(chosen_path() == Path::kSimt ? launch_ctx_simt(c, s) : launch_ctx_tc(c, dev.sm_count, s));
         if (rc != GR_OK) return rc;
     }
     if ((rc = mark(1)) != GR_OK) return rc;

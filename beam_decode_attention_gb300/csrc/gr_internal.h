@@ -114,7 +114,7 @@ cudaError_t launch_ctx_simt(const CtxArgs &a, cudaStream_t s);
 int tc_beams_per_tile(int G);
 int tc_fused_max_steps(int G);  // the fused epilogue holds chains of steps < this
 int tc_merge_max_splits();      // the in-kernel split merge takes at most this many splits
-cudaError_t launch_ctx_tc(const CtxArgs &a, cudaStream_t s);
+cudaError_t launch_ctx_tc(const CtxArgs &a, int sm_count, cudaStream_t s);
 
 // gr_ctx_pk.cu  (persistent tensor-core kernel: the whole call over 128-row tiles, one key split)
 int pk_max_steps();   // chains of steps < this
