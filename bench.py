@@ -784,7 +784,7 @@ def attention_run(gr, torch, spec, steps, warmup, soak_s=0.0, clocks=None):
 def main():
     args = parse_args()
     if args.gpus != 1:
-        print(json.dumps({"error": "this build runs on one GPU; --gpus must be 1"}))
+        print(json.dumps({"error": "every call runs on one GPU (independent requests: replicas only); --gpus must be 1"}))
         return 2
     if args.op == "beam_select":
         return run_select_bench(args)
