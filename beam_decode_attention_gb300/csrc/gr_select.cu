@@ -62,6 +62,7 @@ constexpr int kSide = kHistBins / 2;  // 8-byte entries the histogram's space ho
 constexpr int kMergeThreads = 1024;
 constexpr int kMaxSel = 1024;         // GR_SELECT_MAX_WIDTH
 constexpr int kBoundSlots = 32;       // per-request slots of rows' k-th score keys
+constexpr float kGuessMargin = 0.5f;  // slack of the guessed threshold (logit units)
 
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 
@@ -546,6 +547,20 @@ __device__ __forceinline__ int warp_slots(int cnt, int *wcnt) {
     return base + incl - cnt;
 }
 
+// Warp 0 reads the request's bound so far: the largest published L-th key,
+// and the smallest slot once every slot is set (0: none).
+__device__ __forceinline__ void read_bound(const RowArgs &a, int row, unsigned *out) {
+    const int lane = threadIdx.x & 31;
+    const int req = row / a.W;
+    uint32_t v = lane < a.nslot ? *reinterpret_cast<volatile unsigned *>(a.tau_slot + req * a.nslot + lane) : ~0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFullMask, v, o));
+    if (lane == 0) {
+        const uint32_t l = *reinterpret_cast<volatile unsigned *>(a.tau_lb + req);
+        *out = max(a.nslot > 0 ? v : 0u, l);
+    }
+}
+
 __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kernel(RowArgs a) {
     extern __shared__ unsigned long long sel_smem[];
     unsigned long long *cand = sel_smem;                          // [kCap]
@@ -556,6 +571,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
     __shared__ int s_wcnt[kRowWarps];   // candidates of each warp's region
     __shared__ float s_c;
     __shared__ unsigned s_lb;
+    __shared__ int s_npre;
     const int warp = threadIdx.x >> 5;
     unsigned long long *wreg = cand + warp * kWarpCap;   // this warp's region
 
@@ -575,28 +591,76 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         }
         for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
         if (threadIdx.x < kRowWarps) s_wcnt[threadIdx.x] = 0;
+        if (threadIdx.x == 0) s_npre = 0;
+        if (a.tau_lb && warp == 0) read_bound(a, row, &s_lb);
         __syncthreads();
+        // the prefix's exponentials, against the thread's maximum so far
+        float acc = 0.f;
+        if (mt != -INFINITY) {
+            const float off = -mt * kLog2e;
 #pragma unroll
-        for (int k = 0; k < kFirst; ++k)
-            if (threadIdx.x + k * (int)blockDim.x < F) atomicAdd(&hist[ord_key(xf[k]) >> (32 - kHistBits)], 1);
-        __syncthreads();
-        const int need_s = a.V <= F ? a.L : min(F, 2 * (int)(((long long)F * a.L + a.V - 1) / a.V) + 16);
-        find_bin_call(hist, need_s, red, &s_bin, &s_above);
-        const uint32_t b_hi = (uint32_t)s_bin;
-        const int need_lo = need_s - s_above;
-        __syncthreads();
-        for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kFirst; ++k) {
-            const uint32_t key = ord_key(xf[k]);
-            if (threadIdx.x + k * (int)blockDim.x < F && (key >> 20) == b_hi) atomicAdd(&hist[(key >> 8) & 0xfffu], 1);
+            for (int k = 0; k < kFirst; ++k) acc += ex2_approx(fmaf(xf[k], kLog2e, off));
         }
-        __syncthreads();
-        find_bin_call(hist, need_lo, red, &s_bin, &s_above);
-        const uint32_t tau_key = (b_hi << 20) | ((uint32_t)s_bin << 8);
-        // keys at or below 0x7fffff hold -inf and NaN patterns: no threshold there
-        const float tau = tau_key <= 0x7fffffu ? -INFINITY : key_float(tau_key);
+        // With a bound on the request's W'-th score, the threshold is guessed
+        // from it: a logit reaches the bound when z >= bound - S + c, and the
+        // row's log-normaliser c is estimated from the prefix's as
+        // c_pre + ln(V / F), less a margin.  The guess is taken when the
+        // prefix predicts at most kCap / 2 candidates for the row, otherwise
+        // the histogram's threshold; either way the completeness check after
+        // the stream decides with the row's own c (a guess set too high fails
+        // it, and the row takes the exact path).
+        float tau = -INFINITY;
+        bool by_bound = false;
+        const uint32_t lb0 = a.tau_lb ? s_lb : 0u;
+        if (lb0 != 0u && a.V > F) {
+            MaxSum ms{mt, acc};
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                MaxSum other{__shfl_xor_sync(kFullMask, ms.m, o), __shfl_xor_sync(kFullMask, ms.s, o)};
+                ms = ms_merge(ms, other);
+            }
+            if ((threadIdx.x & 31) == 0) s_ms[warp] = ms;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                MaxSum t = s_ms[0];
+                for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
+                s_c = t.m + __logf(t.s) + __logf((float)a.V / (float)F);
+            }
+            __syncthreads();
+            const float lbs = key_float(lb0), ce = s_c;
+            const float tb = (lbs - S + ce) - (kGuessMargin + 1e-3f * (fabsf(lbs) + fabsf(S) + fabsf(ce)));
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kFirst; ++k) cnt += (threadIdx.x + k * (int)blockDim.x < F && xf[k] >= tb) ? 1 : 0;
+            cnt = __reduce_add_sync(kFullMask, cnt);
+            if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(&s_npre, cnt);
+            __syncthreads();
+            by_bound = isfinite(tb) && (long long)s_npre * a.V <= (long long)(kCap / 2) * F;
+            tau = tb;
+        }
+        if (!by_bound) {
+#pragma unroll
+            for (int k = 0; k < kFirst; ++k)
+                if (threadIdx.x + k * (int)blockDim.x < F) atomicAdd(&hist[ord_key(xf[k]) >> (32 - kHistBits)], 1);
+            __syncthreads();
+            const int need_s = a.V <= F ? a.L : min(F, 2 * (int)(((long long)F * a.L + a.V - 1) / a.V) + 16);
+            find_bin_call(hist, need_s, red, &s_bin, &s_above);
+            const uint32_t b_hi = (uint32_t)s_bin;
+            const int need_lo = need_s - s_above;
+            __syncthreads();
+            for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) hist[i] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kFirst; ++k) {
+                const uint32_t key = ord_key(xf[k]);
+                if (threadIdx.x + k * (int)blockDim.x < F && (key >> 20) == b_hi) atomicAdd(&hist[(key >> 8) & 0xfffu], 1);
+            }
+            __syncthreads();
+            find_bin_call(hist, need_lo, red, &s_bin, &s_above);
+            const uint32_t tau_key = (b_hi << 20) | ((uint32_t)s_bin << 8);
+            // keys at or below 0x7fffff hold -inf and NaN patterns: no threshold there
+            tau = tau_key <= 0x7fffffu ? -INFINITY : key_float(tau_key);
+        }
         {
             int cnt = 0;
 #pragma unroll
@@ -610,13 +674,6 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
                     ++slot;
                 }
             }
-        }
-        // the prefix's exponentials, against the thread's maximum so far
-        float acc = 0.f;
-        if (mt != -INFINITY) {
-            const float off = -mt * kLog2e;
-#pragma unroll
-            for (int k = 0; k < kFirst; ++k) acc += ex2_approx(fmaf(xf[k], kLog2e, off));
         }
 
         // 2. the rest of the row, once: 16-byte loads where the row allows
@@ -746,18 +803,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         // smallest slot once every slot is set (0: none)
         uint32_t lb = 0u;
         if (a.tau_lb) {
-            if (warp == 0) {
-                const int lane = threadIdx.x & 31;
-                const int req = row / a.W;
-                uint32_t v = lane < a.nslot ? *reinterpret_cast<volatile unsigned *>(a.tau_slot + req * a.nslot + lane)
-                                            : ~0u;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFullMask, v, o));
-                if (lane == 0) {
-                    const uint32_t l = *reinterpret_cast<volatile unsigned *>(a.tau_lb + req);
-                    s_lb = max(a.nslot > 0 ? v : 0u, l);
-                }
-            }
+            if (warp == 0) read_bound(a, row, &s_lb);
             __syncthreads();
             lb = s_lb;
         }
