@@ -572,8 +572,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
     __shared__ float s_c;
     __shared__ unsigned s_lb;
     __shared__ int s_npre;
+    __shared__ float s_cpre, s_corr;   // the prefix's log-normaliser; c - c_pre of the last row with a bound
     const int warp = threadIdx.x >> 5;
     unsigned long long *wreg = cand + warp * kWarpCap;   // this warp's region
+    if (threadIdx.x == 0) s_corr = 0.f;
 
     for (int row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const float *z = a.logits + (long long)row * a.V;
@@ -603,12 +605,14 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
         }
         // With a bound on the request's W'-th score, the threshold is guessed
         // from it: a logit reaches the bound when z >= bound - S + c, and the
-        // row's log-normaliser c is estimated from the prefix's as
-        // c_pre + ln(V / F), less a margin.  The guess is taken when the
-        // prefix predicts at most kCap / 2 candidates for the row, otherwise
-        // the histogram's threshold; either way the completeness check after
-        // the stream decides with the row's own c (a guess set too high fails
-        // it, and the row takes the exact path).
+        // row's log-normaliser c is estimated as the prefix's c_pre plus the
+        // difference c - c_pre this CTA saw on its last row that had a bound
+        // (0 before: c >= c_pre, so that guess is always safe), less a
+        // margin.  The guess is taken when the prefix predicts at most kCap / 2
+        // candidates for the row, otherwise the histogram's threshold; either
+        // way the completeness check after the stream decides with the row's
+        // own c (a guess set too high fails it, and the row takes the exact
+        // path).
         float tau = -INFINITY;
         bool by_bound = false;
         const uint32_t lb0 = a.tau_lb ? s_lb : 0u;
@@ -624,7 +628,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
             if (threadIdx.x == 0) {
                 MaxSum t = s_ms[0];
                 for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
-                s_c = t.m + __logf(t.s) + __logf((float)a.V / (float)F);
+                s_cpre = t.m + __logf(t.s);
+                s_c = s_cpre + s_corr;
             }
             __syncthreads();
             const float lbs = key_float(lb0), ce = s_c;
@@ -772,6 +777,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
             MaxSum t = s_ms[0];
             for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = ms_merge(t, s_ms[w]);
             s_c = t.m + __logf(t.s);   // log-normaliser c_b
+            // the prefix's share of the normaliser, for the next row's guess
+            if (lb0 != 0u && a.V > F && isfinite(s_c - s_cpre)) s_corr = s_c - s_cpre;
         }
         __syncthreads();
         const float c = s_c;
