@@ -16,6 +16,9 @@
 //                 twice the share of the row's L best (L = min(W', V)) that
 //                 a prefix of that length holds, by a histogram of their
 //                 ordered bit patterns and a refinement inside its boundary bin;
+//                 or, once the request has a bound on its W'-th score (below),
+//                 a threshold guessed from the bound and the row's estimated
+//                 log-normaliser;
 //   the stream    gives the row's maximum and sum of exponentials and keeps
 //                 every logit at or above the threshold in shared memory;
 //   the select    turns the kept logits into scores and finds the row's L-th
