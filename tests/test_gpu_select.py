@@ -128,6 +128,24 @@ def test_threshold_prefix_skews(skew):
     check(z, inp["beam_scores"], n, par, tok, sco)
 
 
+def test_guessed_threshold_after_an_unlike_row():
+    """More rows than the row kernel has CTAs (four per SM), so each CTA
+    streams rows one after another: flat rows first, then rows whose first
+    4096 logits are raised by 6.  Once the request has a bound, a row's
+    threshold is guessed from it with the normaliser correction (c - c_pre)
+    the CTA saw on its previous row; for a raised row after a flat one that
+    guess is too high, so the completeness check must send the row to a
+    complete k-th selection or the exact path.  The selection stays exact."""
+    grid = torch.cuda.get_device_properties(0).multi_processor_count * 4
+    R, V, n = 1, 20000, 256
+    W = 3 * grid
+    inp = workloads.make_select_inputs(R, W, V, seed=77)
+    z = inp["logits"]
+    z[:, 2 * grid:, :4096] += np.float32(6.0)
+    par, tok, sco, _ = run_select(z, inp["beam_scores"], n)
+    check(z, inp["beam_scores"], n, par, tok, sco)
+
+
 def test_masked_tokens_and_width_past_the_finite_candidates():
     """-inf logits mask tokens; asking for more beams than there are finite
     candidates returns the finite ones by score, then masked ones by index."""
