@@ -908,6 +908,55 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSm) select_rows_kern
     }
 }
 
+// Descending bitonic sort of a warp's 256 entries, eight per lane (entry
+// 8 * lane + j in e[j]): the exchanges below 8 inside a lane, the rest by
+// warp shuffles.  All 32 lanes take part.
+__device__ __forceinline__ void warp_sort256_desc(unsigned long long (&e)[8], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            if (jj >= 8) {
+                const int m = jj >> 3;
+                const bool lower = (lane & m) == 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = 8 * lane + j;
+                    const bool desc = (i & k) == 0;
+                    const unsigned long long o = shfl_xor_u64(e[j], m);
+                    const bool take_max = desc == lower;
+                    e[j] = take_max ? (o > e[j] ? o : e[j]) : (o < e[j] ? o : e[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int pj = j ^ jj;
+                    if (pj > j) {
+                        const int i = 8 * lane + j;
+                        const bool desc = (i & k) == 0;
+                        const unsigned long long lo = e[j], hi = e[pj];
+                        const bool sw = desc ? (lo < hi) : (lo > hi);
+                        e[j] = sw ? hi : lo;
+                        e[pj] = sw ? lo : hi;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// A list tail of n <= 256 entries sorted descending in place by one warp
+// (out of line: the merge kernel's rare overflow path).
+__device__ __noinline__ void sort_tail_in_place(unsigned long long *t, int n, int lane) {
+    unsigned long long e8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) e8[j] = 8 * lane + j < n ? t[8 * lane + j] : 0ull;
+    warp_sort256_desc(e8, lane);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (8 * lane + j < n) t[8 * lane + j] = e8[j];
+}
+
 struct MergeSelArgs {
     const unsigned long long *lists;
     const unsigned *tau_lb;
@@ -928,7 +977,17 @@ struct MergeSelArgs {
     // node, so the order is the same), which also names the child node
     unsigned flat_mul;
     int edge_coded;
+    // > 0 (item-constrained rows): a list that holds every candidate of its
+    // row has its first head_sorted entries in order and the rest in none
+    int head_sorted;
 };
+
+// The merge's head keys per list (their next_width-th largest bounds the
+// request's next_width-th score) and whether they fit its shared memory.
+__host__ __device__ inline int merge_head_keys(int W, int next_width) {
+    const int k = (8 * next_width + W - 1) / W;
+    return k < 1 ? 1 : (k > 32 ? 32 : k);
+}
 
 // dynamic shared memory of the merge kernel: list offsets, per-list counts
 // above and tied with the threshold, the histogram and the selection
@@ -965,7 +1024,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     // of every list (real candidates, so at least next_width entries reach it),
     // to its top 24 bits: a radix select of two 12-bit passes, the key's low 8
     // bits left zero (a lower bound still, looser by at most one 256-ulp bin).
-    const int kh = min(32, max(1, (8 * a.next_width + a.W - 1) / a.W));
+    const int kh = merge_head_keys(a.W, a.next_width);
     // the keys go where offs, gtc and eqc will be (not yet in use)
     const unsigned *heads = reinterpret_cast<const unsigned *>(offs);
     const bool have_heads = a.W * kh <= 3 * (kMaxBeams + 1);
@@ -1013,11 +1072,21 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
     // offsets are written after it.
     int pl[4] = {0, 0, 0, 0};
     int mine = 0;
+    unsigned pend = 0u;   // lists (bit q) whose tail past the head keys is in no order and may reach the bound
+    auto search = [&](int b, int lo) {   // first index at or past lo whose key < lb (sorted list)
+        const unsigned long long *lst = lists + (long long)b * a.L;
+        int hi = plen[b];
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((uint32_t)(lst[mid] >> 32) >= lb) lo = mid + 1;
+            else hi = mid;
+        }
+        return lo;
+    };
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int b = b0 + q;
         if (b >= b1) break;
-        const unsigned long long *lst = lists + (long long)b * a.L;
         const int len = plen[b];
         int lo = 0;
         if (have_heads) {
@@ -1028,30 +1097,88 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
                 mine += lo;
                 continue;
             }
+            if (a.head_sorted) {
+                pl[q] = kh;
+                mine += kh;
+                pend |= 1u << q;
+                continue;
+            }
         }
-        int hi = len;   // first index whose key < lb
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((uint32_t)(lst[mid] >> 32) >= lb) lo = mid + 1;
-            else hi = mid;
-        }
-        pl[q] = lo;
-        mine += lo;
+        pl[q] = search(b, lo);
+        mine += pl[q];
     }
     int total;
-    int off = block_excl_scan(mine, red, &total);
-    __syncthreads();   // every head key has been read
+    auto write_offsets = [&]() {
+        int off = block_excl_scan(mine, red, &total);
+        __syncthreads();   // every head key has been read
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int b = b0 + q;
-        if (b >= b1) break;
-        offs[b] = off;
-        off += pl[q];
-        gtc[b] = 0;
-        eqc[b] = 0;
+        for (int q = 0; q < 4; ++q) {
+            const int b = b0 + q;
+            if (b >= b1) break;
+            offs[b] = off;
+            off += pl[q];
+            gtc[b] = 0;
+            eqc[b] = 0;
+        }
+        if (threadIdx.x == 0) offs[a.W] = total;
+        __syncthreads();
+    };
+    write_offsets();
+    // Lists whose head keys all reach the bound and whose tails are in no
+    // order (item-constrained rows; about one per request): their tail
+    // entries at or above the bound go after the prefixes, filtered by a warp
+    // per list.  If the candidates then overflow the shared memory, the
+    // tails are sorted in place instead and taken into the prefixes.
+    int ntail = 0;
+    if (a.head_sorted) {
+        int *pend_list = hist;   // free until the selection below
+        if (threadIdx.x == 0) {
+            s_bin = 0;
+            s_above = 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (pend >> q & 1u) pend_list[atomicAdd(&s_bin, 1)] = b0 + q;
+        __syncthreads();
+        const int npend = s_bin;
+        const int wq = threadIdx.x >> 5, ln = threadIdx.x & 31, nwq = blockDim.x >> 5;
+        for (int pi = wq; pi < npend; pi += nwq) {
+            const int b = pend_list[pi];
+            const unsigned long long *lst = lists + (long long)b * a.L;
+            const int len = plen[b];
+            for (int j = kh + ln; j < len; j += 32) {
+                const unsigned long long v = lst[j];
+                if ((uint32_t)(v >> 32) >= lb) {
+                    const int pos = atomicAdd(&s_above, 1);
+                    if (total + pos < kEntCap) {
+                        const uint32_t flat = (uint32_t)b * a.flat_mul + ~(uint32_t)v;
+                        ent[total + pos] = ((v >> 32) << 32) | (uint32_t)~flat;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        ntail = s_above;
+        if (npend > 0 && total + ntail > kEntCap) {
+            for (int pi = wq; pi < npend; pi += nwq) {   // warp-uniform
+                const int b = pend_list[pi];
+                // the workspace's list; its tail holds at most 256 - kh entries (a warp row)
+                sort_tail_in_place(const_cast<unsigned long long *>(lists) + (long long)b * a.L + kh, plen[b] - kh, ln);
+            }
+            __syncthreads();   // the sorted tails are visible to the block
+            mine = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int b = b0 + q;
+                if (b >= b1) break;
+                if (pend >> q & 1u) pl[q] = search(b, kh);
+                mine += pl[q];
+            }
+            write_offsets();
+            ntail = 0;
+        }
     }
-    if (threadIdx.x == 0) offs[a.W] = total;
-    __syncthreads();
     // entry e of the flat range: list b (offs[b] <= e < offs[b+1]) and index j
     auto locate = [&](int e, int &b, int &j) {
         int lo = 0, hi = a.W;   // the last b with offs[b] <= e
@@ -1105,7 +1232,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
             if (a.next_node) a.next_node[(long long)r * a.next_width + j] = nd;
         }
     };
-    if (total <= kEntCap) {
+    if (total + ntail <= kEntCap) {
         // Every candidate at or above the bound fits in shared memory: read each
         // once as (score key, ~flat index) and sort them in registers (up to
         // kMaxSel of them; past that only those at or above the n_sel-th
@@ -1119,6 +1246,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
             ent[e] = ((v >> 32) << 32) | (uint32_t)~flat;
         }
         __syncthreads();
+        total += ntail;   // the filtered tails follow the prefixes
         const int n_sel = min(a.next_width, total);
         int n = total;
         if (n > kMaxSel && n_sel > 0) {
@@ -1253,6 +1381,7 @@ struct TrieRowArgs {
     int *big_rows;               // [R * W_s] those rows, in any order
     int rows, W, V, next_width, num_nodes, num_edges;
     int edge_coded;              // list entries carry the edge index instead of the token
+    int head_sorted;             // > 0: a row keeping every candidate orders only its best head_sorted
 };
 
 // A row's trie node and its edge range [p0, p1) (empty for a node index or
@@ -1323,29 +1452,28 @@ __global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(Trie
         e[j] = v[j] >= 0 ? pack(ord_key(score_of(x[j], c, S)),
                                 ~(uint32_t)(a.edge_coded ? p0 + 8 * lane + j : v[j]))
                          : 0ull;
-    // descending bitonic sort of the warp's 256 elements (index i = 8 * lane + j)
+    // the valid candidates (a skipped edge is 0, below every score)
+    int valid = 0;
 #pragma unroll
-    for (int k = 2; k <= kTrieWarpDeg; k <<= 1) {
+    for (int j = 0; j < 8; ++j) valid += (e[j] >> 32) != 0ull ? 1 : 0;
 #pragma unroll
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            if (jj >= 8) {
-                const int m = jj >> 3;
-                const bool lower = (lane & m) == 0;
+    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(kFullMask, valid, o);
+    unsigned long long *out = a.lists + (long long)row * a.next_width;
+    if (a.head_sorted > 0 && valid < a.next_width) {   // warp-uniform
+        // The row keeps every candidate, and the merge reads in order only
+        // its first head_sorted: those in order, the rest in none.  Each
+        // lane sorts its eight, then every round takes the warp's largest
+        // head (entries are distinct: one lane holds it) and that lane
+        // moves up its next.
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = 8 * lane + j;
-                    const bool desc = (i & k) == 0;
-                    const unsigned long long o = shfl_xor_u64(e[j], m);
-                    const bool take_max = desc == lower;
-                    e[j] = take_max ? (o > e[j] ? o : e[j]) : (o < e[j] ? o : e[j]);
-                }
-            } else {
+        for (int k = 2; k <= 8; k <<= 1) {
+#pragma unroll
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int pj = j ^ jj;
                     if (pj > j) {
-                        const int i = 8 * lane + j;
-                        const bool desc = (i & k) == 0;
+                        const bool desc = (j & k) == 0;
                         const unsigned long long lo = e[j], hi = e[pj];
                         const bool sw = desc ? (lo < hi) : (lo > hi);
                         e[j] = sw ? hi : lo;
@@ -1354,15 +1482,42 @@ __global__ void __launch_bounds__(kTrieWarpRows * 32) trie_rows_warp_kernel(Trie
                 }
             }
         }
+        const int T = min(a.head_sorted, valid);
+        unsigned long long top = 0ull;
+        for (int rr = 0; rr < T; ++rr) {
+            unsigned long long h = e[0];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long x = shfl_xor_u64(h, o);
+                h = x > h ? x : h;
+            }
+            if (lane == rr) top = h;
+            const bool win = e[0] == h;
+#pragma unroll
+            for (int j = 0; j < 7; ++j) e[j] = win ? e[j + 1] : e[j];
+            e[7] = win ? 0ull : e[7];
+        }
+        if (lane < T) out[lane] = top;
+        // the rest: each lane's remaining valid entries (first in e[]), after those of the lanes before it
+        int mine = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine += (e[j] >> 32) != 0ull ? 1 : 0;
+        int pre = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(kFullMask, pre, o);
+            if (lane >= o) pre += x;
+        }
+        pre -= mine;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < mine) out[T + pre + j] = e[j];
+        if (lane == 0) a.plen[row] = valid;
+        return;
     }
-    // the kept count: valid candidates, at most W'
-    int valid = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) valid += (e[j] >> 32) != 0ull ? 1 : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(kFullMask, valid, o);
+    // descending sort of the warp's 256 entries (entry 8 * lane + j in e[j])
+    warp_sort256_desc(e, lane);
     const int cnt = min(valid, a.next_width);
-    unsigned long long *out = a.lists + (long long)row * a.next_width;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         if (8 * lane + j < cnt) out[8 * lane + j] = e[j];
@@ -1632,6 +1787,12 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ta.big_rows = big_rows;
     // edge-coded entries while every flat index b * num_edges + e fits 32 bits
     ta.edge_coded = (num_edges > 0 && (unsigned long long)W * (unsigned long long)num_edges < (1ull << 32)) ? 1 : 0;
+    // rows that keep every candidate order only the merge's head keys when
+    // those fit its shared memory and are few (a full sort is cheaper past 8)
+    {
+        const int kh = merge_head_keys(W, next_width);
+        ta.head_sorted = ((long long)W * kh <= 3LL * (kMaxBeams + 1) && kh <= 8) ? kh : 0;
+    }
     trie_rows_warp_kernel<<<(R * W + kTrieWarpRows - 1) / kTrieWarpRows, kTrieWarpRows * 32, 0, s>>>(ta);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1647,6 +1808,7 @@ cudaError_t launch_trie_select(int R, int W, int V, int next_width, int num_node
     ma.lists = ta.lists;
     ma.tau_lb = tau_lb;
     ma.plen = plen;
+    ma.head_sorted = ta.head_sorted;
     ma.W = W;
     ma.V = V;
     ma.L = next_width;

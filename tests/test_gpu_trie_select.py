@@ -126,6 +126,26 @@ def test_rows_wide_and_narrow_in_one_request():
     check(inp["logits"], inp["beam_scores"], bn, t["offsets"], t["tokens"], t["children"], 40, got)
 
 
+def test_exact_ties_overflow_the_merge_buffer():
+    """Every candidate ties exactly (equal legal logits, equal beam scores):
+    a row list orders only its head entries, every list's head reaches the
+    merge's bound, and the candidates at or above it (12,800) overflow the
+    merge's shared memory.  The rows' unordered tails are then sorted in
+    place and the lists walked where they are; the selection is the
+    flat-index order."""
+    W, V, deg, n = 64, 300, 200, 64
+    offsets = np.array([0] + [deg] * (deg + 1), dtype=np.int32)   # the root's deg edges, then deg leaves
+    tokens = np.arange(deg, dtype=np.int32)
+    children = np.arange(1, deg + 1, dtype=np.int32)
+    logits = np.zeros((1, W, V), np.float32)
+    scores = np.full((1, W), -1.0, np.float32)
+    beam_node = np.zeros((1, W), np.int32)
+    par, tok, nod, sco = run(logits, scores, beam_node, offsets, tokens, children, n)
+    assert np.array_equal(par[0], np.zeros(n)) and np.array_equal(tok[0], np.arange(n))
+    assert np.array_equal(nod[0], np.arange(1, n + 1))
+    assert np.allclose(sco[0], -1.0 - np.log(deg), atol=1e-5)
+
+
 def test_out_of_range_nodes_are_skipped():
     """Beams whose node index lies outside the trie contribute nothing (the
     kernel checks the index before reading the trie)."""
