@@ -978,7 +978,9 @@ struct MergeSelArgs {
     unsigned flat_mul;
     int edge_coded;
     // > 0 (item-constrained rows): a list that holds every candidate of its
-    // row has its first head_sorted entries in order and the rest in none
+    // row has its first head_sorted entries in order and the rest in none.
+    // Set only when head_sorted equals the merge's head keys per list and
+    // those fit its shared memory (the prefixes are then read from them).
     int head_sorted;
 };
 
@@ -1163,7 +1165,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) select_merge_kernel(MergeSel
         if (npend > 0 && total + ntail > kEntCap) {
             for (int pi = wq; pi < npend; pi += nwq) {   // warp-uniform
                 const int b = pend_list[pi];
-                // the workspace's list; its tail holds at most 256 - kh entries (a warp row)
+                // the workspace's list: a warp row's tail holds at most 256 - kh
+                // entries; a wide row's list is in order already, and sorting the
+                // first 256 entries of its tail keeps it so
                 sort_tail_in_place(const_cast<unsigned long long *>(lists) + (long long)b * a.L + kh, plen[b] - kh, ln);
             }
             __syncthreads();   // the sorted tails are visible to the block
