@@ -465,7 +465,7 @@ def run_trie_bench(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": conf,
         "roofline": {"bound": "hbm", "achieved": round(alg / (value * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(alg / (value * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
-                     "traffic": None,
+                     "traffic": recorded_traffic(conf["workload"], SELECT_KERNEL_SOURCES),
                      "kernel": "whole call (trie_rows_warp_kernel, trie_rows_kernel, select_merge_kernel)",
                      "peak_source": pk.get("source", "measured copy")},
         "gpu_launches": 3 * args.steps, "clocks": clk, "cpu_baseline": None, "e2e": None,
