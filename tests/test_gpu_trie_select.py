@@ -126,6 +126,25 @@ def test_rows_wide_and_narrow_in_one_request():
     check(inp["logits"], inp["beam_scores"], bn, t["offsets"], t["tokens"], t["children"], 40, got)
 
 
+def test_rows_with_fewer_and_more_candidates_than_the_width():
+    """Beams at a node of 16 edges keep every candidate (fewer than W' = 20:
+    only the merge's head keys are put in order), beams at a node of 30 edges
+    keep their best 20 in full order and publish their 20th as a bound; both
+    kinds of list feed one merge."""
+    V, W, n = 64, 40, 20
+    # node 0: the root (edges to nodes 1 and 2); node 1: 16 edges; node 2: 30 edges; nodes 3..48: leaves
+    deg = [2, 16, 30]
+    offsets = np.concatenate([[0], np.cumsum(deg), np.full(46, sum(deg))]).astype(np.int32)
+    tokens = np.concatenate([[0, 1], np.arange(10, 26), np.arange(30, 60)]).astype(np.int32)
+    children = np.concatenate([[1, 2], np.arange(3, 19), np.arange(19, 49)]).astype(np.int32)
+    rng = np.random.default_rng(2020)
+    logits = (rng.standard_normal(size=(2, W, V)) * 2.0).astype(np.float32)
+    scores = (-np.abs(rng.standard_normal(size=(2, W))) * 3.0).astype(np.float32)
+    beam_node = np.where(np.arange(W) % 2 == 0, 1, 2)[None, :].repeat(2, axis=0).astype(np.int32)
+    got = run(logits, scores, beam_node, offsets, tokens, children, n)
+    check(logits, scores, beam_node, offsets, tokens, children, n, got)
+
+
 def test_exact_ties_overflow_the_merge_buffer():
     """Every candidate ties exactly (equal legal logits, equal beam scores):
     a row list orders only its head entries, every list's head reaches the
